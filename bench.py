@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the MMVQ hot path on GB300: weight GB/s per call at 1-8 columns.
+
+Default workload: the Q6_K sweep -- 2560x2560, 2560x10240 and 10240x2560
+(rows x K) at 1, 2, 4, 6 and 8 Q8_1 columns, weights repacked at load into
+planar tiles -- the pages' mmvq_bench table ("Strata" PR #2207).  One step
+is one pass over every (shape, columns) case on every resident copy of its
+matrix; the copies of each shape total more than twice the L2 size, so no
+call finds its weights in L2.  Each call is the hot path: Q8_1 quantisation
+of the fp32 columns, then the MMVQ kernel.
+
+The step's calls are made through the public binding and captured once as a
+CUDA graph (the pages' figures are graph replays too, PR #2746), with an
+event-record node around every kernel, so every kernel's duration comes
+from the timed region itself.  `value` = weight bytes of all calls / device
+time; `e2e` repeats the step with the fp32 columns copied in from pinned
+host memory and all outputs read back every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a row sample
+
+Under torchrun each rank runs an independent replica (the path has no
+exchange step); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+METRIC = "weight GB/s per MMVQ call (fraction of HBM peak) and us/call at 1-8 cols"
+UNIT = "GB/s"
+
+SWEEP_SHAPES = [(2560, 2560), (2560, 10240), (10240, 2560)]
+SWEEP_COLS = [1, 2, 4, 6, 8]
+HEAD_SHAPE = (151936, 2560)
+Q4K_SHAPES = [(12288, 2560), (6144, 2560), (2560, 6144), (640, 2560), (512, 2560)]
+
+
+def workload_cases(name):
+    """-> list of (fmt, rows, K, ncols_list)."""
+    if name == "q6k_sweep":
+        return [("q6_k_planar", r, k, SWEEP_COLS) for r, k in SWEEP_SHAPES]
+    if name == "q6k_sweep_gguf":
+        return [("q6_k", r, k, SWEEP_COLS) for r, k in SWEEP_SHAPES]
+    if name == "lm_head":
+        return [("q6_k_planar", HEAD_SHAPE[0], HEAD_SHAPE[1], [1, 2, 3, 4, 5])]
+    if name == "q4k_dense":
+        return [("q4_k", r, k, [1, 4]) for r, k in Q4K_SHAPES]
+    raise SystemExit(f"unknown workload {name}")
+
+
+WORKLOAD_DESC = {
+    "q6k_sweep": "Q6_K MMVQ sweep 2560x2560, 2560x10240, 10240x2560 (rows x K) at 1,2,4,6,8 cols, planar tiles",
+    "q6k_sweep_gguf": "Q6_K MMVQ sweep 2560x2560, 2560x10240, 10240x2560 at 1,2,4,6,8 cols, GGUF blocks",
+    "lm_head": "Q6_K LM head 151936x2560 at 1-5 cols, planar tiles",
+    "q4k_dense": "Q4_K dense 12288x2560, 6144x2560, 2560x6144, 640x2560, 512x2560 at 1 and 4 cols",
+}
+
+
+def load_peak():
+    p = os.path.join(HERE, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- graph events --
+
+_cudart = None
+
+
+def _record_external(ev, stream):
+    """Event-record node inside a stream capture (cudaEventRecordExternal), so
+    the event is timestamped every time the graph runs."""
+    global _cudart
+    if _cudart is None:
+        _cudart = ctypes.CDLL("libcudart.so.13")
+        _cudart.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        _cudart.cudaEventRecordWithFlags.restype = ctypes.c_int
+    rc = _cudart.cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event),
+                                          ctypes.c_void_p(stream.cuda_stream), 1)
+    if rc != 0:
+        raise RuntimeError(f"cudaEventRecordWithFlags failed ({rc})")
+
+
+# -------------------------------------------------------------- our arm --
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from block_quantized_matvec_gb300 import metrics, mmvq, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    mmvq.lib()
+
+    cases_spec = workload_cases(args.workload)
+    type_of = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K}
+
+    # resident weights: copies per shape so that each shape's copies exceed 2x L2
+    mats = []
+    host_weights = []
+    for si, (fmt, rows, K, cols) in enumerate(cases_spec):
+        gen = synth.q4_k_weights if fmt == "q4_k" else synth.q6_k_weights
+        W = gen(rows, K, salt=si)
+        host_weights.append(W)
+        Wd = torch.from_numpy(W.reshape(-1)).to(dev)
+        if fmt == "q6_k_planar":
+            Wd = mmvq.repack_planar(Wd, rows, K)
+        nbytes = metrics.weight_bytes(fmt, rows, K)
+        copies = max(2, math.ceil(2 * l2 / nbytes)) if not args.no_rotate else 1
+        mats.append([Wd] + [Wd.clone() for _ in range(copies - 1)])
+    torch.cuda.synchronize()
+
+    # activations of every (shape, ncols) case, in one buffer (one H2D per step for e2e)
+    case_list = []
+    x_total = 0
+    for si, (fmt, rows, K, cols) in enumerate(cases_spec):
+        for nc in cols:
+            case_list.append((si, fmt, rows, K, nc, x_total))
+            x_total += nc * K
+    x_host = np.concatenate([synth.activations(K, nc, salt=100 * si + nc).reshape(-1)
+                             for (si, fmt, rows, K, nc, _) in case_list])
+    x_dev = torch.from_numpy(x_host).to(dev)
+    x_pinned = torch.from_numpy(x_host).pin_memory()
+    xq_bufs = [torch.empty((nc, K // 32, 36), dtype=torch.uint8, device=dev)
+               for (_, _, _, K, nc, _) in case_list]
+
+    calls = []  # (case index, copy index, y offset)
+    y_total = 0
+    for ci, (si, fmt, rows, K, nc, xo) in enumerate(case_list):
+        for cp in range(len(mats[si])):
+            calls.append((ci, cp, y_total))
+            y_total += nc * rows
+    y_dev = torch.empty(y_total, dtype=torch.float32, device=dev)
+    y_pinned = torch.empty(y_total, dtype=torch.float32).pin_memory()
+
+    def call(i, stream=None):
+        ci, cp, yo = calls[i]
+        si, fmt, rows, K, nc, xo = case_list[ci]
+        x = x_dev[xo:xo + nc * K].view(nc, K)
+        mmvq.quantize_q8_1(x, out=xq_bufs[ci])
+        mmvq.gemv(type_of[fmt], mats[si][cp], rows, K, xq_bufs[ci], nc,
+                  out=y_dev[yo:yo + nc * rows].view(nc, rows))
+
+    # first calls outside any capture (kernel attributes, occupancy)
+    for i in range(len(calls)):
+        call(i)
+    torch.cuda.synchronize()
+
+    # capture the step with an event node before each kernel and after the last
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(calls) + 1)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+        s = torch.cuda.current_stream()
+        for i in range(len(calls)):
+            ci, cp, yo = calls[i]
+            si, fmt, rows, K, nc, xo = case_list[ci]
+            _record_external(evs[2 * i], s)
+            mmvq.quantize_q8_1(x_dev[xo:xo + nc * K].view(nc, K), out=xq_bufs[ci])
+            _record_external(evs[2 * i + 1], s)
+            mmvq.gemv(type_of[fmt], mats[si][cp], rows, K, xq_bufs[ci], nc,
+                      out=y_dev[yo:yo + nc * rows].view(nc, rows))
+        _record_external(evs[-1], s)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+        dist.barrier()
+
+    # per-kernel durations from the event nodes of the last step
+    q_us = np.array([evs[2 * i].elapsed_time(evs[2 * i + 1]) * 1e3 for i in range(len(calls))])
+    g_us = np.array([evs[2 * i + 1].elapsed_time(evs[2 * i + 2]) * 1e3 for i in range(len(calls))])
+
+    peak, peak_kind = load_peak()
+    w_step = 0
+    alg_step = 0
+    per_case = []
+    for ci, (si, fmt, rows, K, nc, xo) in enumerate(case_list):
+        idx = [i for i, c in enumerate(calls) if c[0] == ci]
+        wb = metrics.weight_bytes(fmt, rows, K)
+        ab = metrics.call_bytes(fmt, rows, K, nc)
+        w_step += wb * len(idx)
+        alg_step += ab * len(idx)
+        gu = float(np.mean(g_us[idx]))
+        qu = float(np.mean(q_us[idx]))
+        per_case.append({"shape": f"{rows}x{K}", "fmt": fmt, "ncols": nc,
+                         "us_per_call": round(gu, 3), "us_quantize": round(qu, 3),
+                         "weight_gbps": round(wb / gu / 1e3, 1),
+                         "frac_of_measured": round(wb / gu / 1e3 / peak, 3)})
+    step_s = elapsed_ms / 1e3 / args.steps
+    value = world * w_step / step_s / 1e9
+    achieved = alg_step / (float(np.sum(g_us)) * 1e-6) / 1e9
+
+    # e2e: H2D of the step's columns, the step, D2H of every output, each step
+    e2e_steps = max(3, min(args.steps, 200))
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_pinned, non_blocking=True)
+        graph.replay()
+        y_pinned.copy_(y_dev, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - w0) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a + fp32",
+        "data": "synthetic (seeded generators shaped like the pages' matrices)",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": len(calls),
+                   "weight_copies": [len(m) for m in mats],
+                   "l2": "weights rotated over copies > 2x L2 per shape (inputs larger than L2)",
+                   "timing": "CUDA graph replay; event nodes around every kernel",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": "mmvq_dense_kernel (all launches of the step)"},
+        "e2e": {"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
+                "steps": e2e_steps},
+        "gpu_launches": 2 * len(calls) * args.steps,
+        "clocks": clk,
+        "cases": per_case,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cases_spec, host_weights, args.cpu_seconds)
+    return out
+
+
+# ---------------------------------------------------------- CPU oracle --
+
+def _oracle_pass(cases_spec, host_weights, row_sample, salt0=0):
+    """One pass of the oracle over every case; returns (weight bytes, seconds)."""
+    import oracle
+    from block_quantized_matvec_gb300 import metrics, synth
+    tcode = {"q6_k_planar": oracle.TYPE_Q6_K, "q6_k": oracle.TYPE_Q6_K, "q4_k": oracle.TYPE_Q4_K}
+    nbytes = 0
+    secs = 0.0
+    for si, (fmt, rows, K, cols) in enumerate(cases_spec):
+        W = host_weights[si]
+        r = rows if row_sample is None else min(rows, row_sample)
+        Ws = W if r == rows else np.ascontiguousarray(W[:r])
+        for nc in cols:
+            x = synth.activations(K, nc, salt=100 * si + nc)
+            t = time.perf_counter()
+            xq = oracle.quantize_q8_1(x)
+            oracle.gemv(tcode[fmt], Ws, r, K, xq, nc)
+            secs += time.perf_counter() - t
+            nbytes += metrics.weight_bytes(fmt, r, K)
+    return nbytes, secs
+
+
+def cpu_baseline(cases_spec, host_weights, seconds):
+    import oracle
+    oracle.build()
+    nb_total, s_total, passes = 0, 0.0, 0
+    while passes < 1 or (s_total < seconds and passes < 50):
+        nb, s = _oracle_pass(cases_spec, host_weights, None)
+        nb_total += nb
+        s_total += s
+        passes += 1
+    return {"value": round(nb_total / s_total / 1e9, 3), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{passes} full pass(es) of every case (all rows, all columns), "
+                      f"{s_total:.1f} s single-threaded on {os.cpu_count()} host cores"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, each step a row sample of every case."""
+    if rank != 0:
+        return None
+    from block_quantized_matvec_gb300 import synth
+    import oracle
+    oracle.build()
+    cases_spec = workload_cases(args.workload)
+    sample_rows = 64
+    host_weights = []
+    for si, (fmt, rows, K, cols) in enumerate(cases_spec):
+        gen = synth.q4_k_weights if fmt == "q4_k" else synth.q6_k_weights
+        host_weights.append(np.ascontiguousarray(gen(min(rows, sample_rows), K, salt=si)))
+    for _ in range(args.warmup):
+        _oracle_pass(cases_spec, host_weights, sample_rows)
+    nb_total, s_total = 0, 0.0
+    for _ in range(args.steps):
+        nb, s = _oracle_pass(cases_spec, host_weights, sample_rows)
+        nb_total += nb
+        s_total += s
+    v = nb_total / s_total / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(s_total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32 + fp32 (oracle)",
+        "data": "synthetic (seeded generators shaped like the pages' matrices)",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "parallelism": "host, 1 thread"},
+        "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"first {sample_rows} rows of every case per step, all columns"},
+        "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="q6k_sweep", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rotate", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

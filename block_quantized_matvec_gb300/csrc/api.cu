@@ -1,0 +1,159 @@
+// C ABI of libmmvq.so (declared in include/mmvq.h).  Every entry point
+// checks its arguments on the host before any CUDA call, then launches
+// asynchronously on the caller's stream.  Nothing is allocated here.
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace mmvq {
+int launch_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq, cudaStream_t s);
+int launch_silu_mul_quantize(const float* gu, int F, int n, void* xq, float* h_out, cudaStream_t s);
+int launch_dense(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
+                 int32_t* sumi, cudaStream_t s);
+int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,
+                   const int32_t* expert_ids, const int32_t* offsets, int n_groups,
+                   const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
+                   int32_t* status, cudaStream_t s);
+int launch_repack_planar(const void* W, int64_t rows, int K, void* P, cudaStream_t s);
+int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_ids, int n,
+                         void* out, int32_t* status, cudaStream_t s);
+int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                        int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
+                        cudaStream_t s);
+}  // namespace mmvq
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_weights_shape(int64_t rows, int K) {
+  if (rows < 1 || rows > 0x7fffffffLL) return MMVQ_ERR_SHAPE;
+  if (K < mmvq::kQK || K > mmvq::kMaxK || K % mmvq::kQK != 0) return MMVQ_ERR_SHAPE;
+  return MMVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mmvq_version(void) { return 10000; }
+
+const char* mmvq_strerror(int code) {
+  switch (code) {
+    case MMVQ_OK: return "ok";
+    case MMVQ_ERR_TYPE: return "unsupported weight type for this call";
+    case MMVQ_ERR_SHAPE: return "bad shape (K must be a multiple of 256, at most 16384; sizes >= 1)";
+    case MMVQ_ERR_NCOLS: return "ncols must be in 1..8";
+    case MMVQ_ERR_NULL: return "a required pointer is NULL";
+    case MMVQ_ERR_ALIGN: return "a pointer breaks its alignment rule (16 B for W/xq/out, 4 B otherwise)";
+    case MMVQ_ERR_ROUTING: return "routing lists rejected";
+    case MMVQ_ERR_CUDA: return "CUDA launch failed (no usable sm_103a device?)";
+  }
+  return "unknown mmvq status";
+}
+
+int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq,
+                       mmvq_stream_t stream) {
+  if (!x || !xq) return MMVQ_ERR_NULL;
+  if (K <= 0 || K % mmvq::kQK8 != 0 || ldx < K || ncols < 1 || ncols > 65535) return MMVQ_ERR_SHAPE;
+  if (!aligned(x, 4) || !aligned(xq, 16)) return MMVQ_ERR_ALIGN;
+  return mmvq::launch_quantize_q8_1(x, K, ncols, ldx, xq, (cudaStream_t)stream);
+}
+
+static int gemv_checks(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
+                       const void* out) {
+  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K && type != MMVQ_Q6_K_PLANAR) return MMVQ_ERR_TYPE;
+  if (!W || !xq || !out) return MMVQ_ERR_NULL;
+  const int rc = check_weights_shape(rows, K);
+  if (rc) return rc;
+  if (ncols < 1 || ncols > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
+  if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(out, 4)) return MMVQ_ERR_ALIGN;
+  return MMVQ_OK;
+}
+
+int mmvq_gemv(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
+              mmvq_stream_t stream) {
+  const int rc = gemv_checks(type, W, rows, K, xq, ncols, y);
+  if (rc) return rc;
+  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, nullptr, (cudaStream_t)stream);
+}
+
+int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
+                          int32_t* sumi, float* y, mmvq_stream_t stream) {
+  const int rc = gemv_checks(type, W, rows, K, xq, ncols, sumi);
+  if (rc) return rc;
+  if (!y) return MMVQ_ERR_NULL;
+  if (!aligned(y, 4)) return MMVQ_ERR_ALIGN;
+  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, sumi, (cudaStream_t)stream);
+}
+
+int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, int K,
+                 const int32_t* expert_ids, const int32_t* token_offsets, int n_groups,
+                 const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
+                 int32_t* status, mmvq_stream_t stream) {
+  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K) return MMVQ_ERR_TYPE;
+  if (!W_experts || !expert_ids || !token_offsets || !xq || !y) return MMVQ_ERR_NULL;
+  int rc = check_weights_shape(rows, K);
+  if (rc) return rc;
+  if (n_experts < 1 || n_xq_cols < 1) return MMVQ_ERR_SHAPE;
+  if (n_groups < 1 || n_groups > 4096) return MMVQ_ERR_ROUTING;
+  if (!aligned(W_experts, 16) || !aligned(xq, 16) || !aligned(y, 4) || !aligned(expert_ids, 4) ||
+      !aligned(token_offsets, 4) || (act_index && !aligned(act_index, 4)) ||
+      (status && !aligned(status, 4)))
+    return MMVQ_ERR_ALIGN;
+  return mmvq::launch_grouped(type, W_experts, n_experts, rows, K, expert_ids, token_offsets,
+                              n_groups, act_index, xq, n_xq_cols, y, status, (cudaStream_t)stream);
+}
+
+int mmvq_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                      int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
+                      int32_t* status, mmvq_stream_t stream) {
+  if (!expert_ids || !token_offsets || !act_index || !slot_of) return MMVQ_ERR_NULL;
+  if (T > 0 && !topk) return MMVQ_ERR_NULL;
+  if (n_experts < 1 || n_experts > 4096 || T < 0 || k < 1 || (int64_t)T * k > 65536)
+    return MMVQ_ERR_SHAPE;
+  if ((topk && !aligned(topk, 4)) || !aligned(expert_ids, 4) || !aligned(token_offsets, 4) ||
+      !aligned(act_index, 4) || !aligned(slot_of, 4) || (status && !aligned(status, 4)))
+    return MMVQ_ERR_ALIGN;
+  return mmvq::launch_route_groups(topk, T, k, n_experts, expert_ids, token_offsets, act_index,
+                                   slot_of, status, (cudaStream_t)stream);
+}
+
+int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq, float* h_out,
+                                mmvq_stream_t stream) {
+  if (!gu || !xq) return MMVQ_ERR_NULL;
+  if (F <= 0 || F % mmvq::kQK8 != 0 || n < 1) return MMVQ_ERR_SHAPE;
+  if (!aligned(gu, 4) || !aligned(xq, 16) || (h_out && !aligned(h_out, 4))) return MMVQ_ERR_ALIGN;
+  return mmvq::launch_silu_mul_quantize(gu, F, n, xq, h_out, (cudaStream_t)stream);
+}
+
+int64_t mmvq_planar_bytes(int64_t rows, int K) {
+  if (check_weights_shape(rows, K) != MMVQ_OK) return -1;
+  const int64_t groups = (rows + mmvq::kTileRows - 1) / mmvq::kTileRows;
+  return groups * (K / mmvq::kQK) * mmvq::kTileBytes;
+}
+
+int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int K, void* W_planar,
+                       mmvq_stream_t stream) {
+  if (type != MMVQ_Q6_K) return MMVQ_ERR_TYPE;
+  if (!W_gguf || !W_planar) return MMVQ_ERR_NULL;
+  const int rc = check_weights_shape(rows, K);
+  if (rc) return rc;
+  if (!aligned(W_gguf, 2) || !aligned(W_planar, 16)) return MMVQ_ERR_ALIGN;
+  return mmvq::launch_repack_planar(W_gguf, rows, K, W_planar, (cudaStream_t)stream);
+}
+
+int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int32_t* row_ids,
+                            int n, void* out, int32_t* status, mmvq_stream_t stream) {
+  if (!W_planar || !row_ids || !out) return MMVQ_ERR_NULL;
+  int rc = check_weights_shape(rows, K);
+  if (rc) return rc;
+  if (n < 1) return MMVQ_ERR_SHAPE;
+  if (!aligned(W_planar, 16) || !aligned(out, 16) || !aligned(row_ids, 4) ||
+      (status && !aligned(status, 4)))
+    return MMVQ_ERR_ALIGN;
+  return mmvq::launch_gather_planar(W_planar, rows, K, row_ids, n, out, status,
+                                    (cudaStream_t)stream);
+}
+
+}  // extern "C"

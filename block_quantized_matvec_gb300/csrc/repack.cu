@@ -1,0 +1,245 @@
+// Load-time planar repack of Q6_K, draft-head row gather, and per-expert
+// token lists from top-k routing.
+//
+// Planar ("Strata" PR #2340 "STRATA_Q6_PLANAR": the head is converted at
+// load into ql / qh / scales / d planes, the same bytes, so each lane's
+// loads are aligned 16-byte loads; the draft head's subset is gathered from
+// the planar head).  Here the planes are kept per 16-row x 256-column tile
+// in the order the MMVQ warps read them (see include/mmvq.h).
+#include "common.cuh"
+
+namespace mmvq {
+
+// What the 16-byte tile chunk q (0..209) holds: `pieces` pieces of `len`
+// bytes, for consecutive tile lanes (or rows, for d) starting at lane0.
+struct ChunkMap {
+  int pieces;     // 1 (16-byte piece), 2 (two 8-byte scale pieces) or 8 (eight d's)
+  int len;        // bytes per piece
+  int lane0;      // first tile lane (ql/qh/scale pieces) or first row (d pieces)
+  int blk_off;    // offset of the piece in the GGUF block for lane0 (h from lane)
+};
+
+__device__ __forceinline__ ChunkMap chunk_map(int q) {
+  ChunkMap m;
+  if (q < 128) {  // ql: j = q/32, lane = q%32 -> ql[64h + 16j]
+    const int j = q >> 5, L = q & 31;
+    m.pieces = 1; m.len = 16; m.lane0 = L; m.blk_off = 64 * (L >> 4) + 16 * j;
+  } else if (q < 192) {  // qh: j = (q-128)/32 -> qh[32h + 16j]
+    const int j = (q - 128) >> 5, L = (q - 128) & 31;
+    m.pieces = 1; m.len = 16; m.lane0 = L; m.blk_off = 128 + 32 * (L >> 4) + 16 * j;
+  } else if (q < 208) {  // scales: lanes 2(q-192), +1 -> scales[8h]
+    const int L = 2 * (q - 192);
+    m.pieces = 2; m.len = 8; m.lane0 = L; m.blk_off = 192 + 8 * (L >> 4);
+  } else {  // d: rows 8(q-208) .. +7
+    m.pieces = 8; m.len = 2; m.lane0 = 8 * (q - 208); m.blk_off = 208;
+  }
+  return m;
+}
+
+// One CTA per tile T(g, b); thread q < 210 writes tile chunk q.
+__global__ void __launch_bounds__(256) repack_planar_kernel(const uint8_t* __restrict__ W,
+                                                            int64_t rows, int nb,
+                                                            uint8_t* __restrict__ P) {
+  const int64_t t = blockIdx.x;
+  const int64_t g = t / nb;
+  const int b = (int)(t - g * nb);
+  const int q = threadIdx.x;
+  if (q >= kTileBytes / 16) return;
+  const ChunkMap m = chunk_map(q);
+  alignas(16) uint8_t buf[16];
+  for (int p = 0; p < m.pieces; ++p) {
+    const int lane_or_row = m.lane0 + p;
+    int i, off;
+    if (m.pieces == 8) {
+      i = lane_or_row;
+      off = m.blk_off;
+    } else {
+      i = lane_or_row & 15;
+      off = (m.pieces == 2) ? 192 + 8 * (lane_or_row >> 4) : m.blk_off;
+    }
+    const int64_t row = g * kTileRows + i;
+    const uint8_t* src = W + (row * nb + b) * kQ6KBytes + off;
+    for (int k = 0; k < m.len; k += 2) {
+      uint16_t v = 0;
+      if (row < rows) v = *reinterpret_cast<const uint16_t*>(src + k);
+      buf[p * m.len + k] = (uint8_t)(v & 0xff);
+      buf[p * m.len + k + 1] = (uint8_t)(v >> 8);
+    }
+  }
+  *reinterpret_cast<uint4*>(P + t * kTileBytes + 16 * q) = *reinterpret_cast<const uint4*>(buf);
+}
+
+// One CTA per output tile; out row k = source row row_ids[k] (zero bytes
+// for k >= n or an invalid id).
+__global__ void __launch_bounds__(256) gather_planar_kernel(const uint8_t* __restrict__ P,
+                                                            int64_t rows, int nb,
+                                                            const int32_t* __restrict__ row_ids,
+                                                            int n, uint8_t* __restrict__ out,
+                                                            int32_t* __restrict__ status) {
+  const int64_t t = blockIdx.x;
+  const int64_t g = t / nb;
+  const int b = (int)(t - g * nb);
+  const int q = threadIdx.x;
+  if (q >= kTileBytes / 16) return;
+  const ChunkMap m = chunk_map(q);
+  alignas(16) uint8_t buf[16];
+  for (int p = 0; p < m.pieces; ++p) {
+    const int lane_or_row = m.lane0 + p;
+    const int i = (m.pieces == 8) ? lane_or_row : (lane_or_row & 15);
+    const int64_t k = g * kTileRows + i;
+    int64_t src_row = -1;
+    if (k < n) {
+      const int32_t r = row_ids[k];
+      if (r >= 0 && r < rows) {
+        src_row = r;
+      } else if (status) {
+        *status = MMVQ_ERR_ROUTING;
+      }
+    }
+    // same section and half in the source tile, the source row's lane
+    int src_off;
+    if (src_row < 0) {
+      for (int k2 = 0; k2 < m.len; ++k2) buf[p * m.len + k2] = 0;
+      continue;
+    }
+    const int si = (int)(src_row % kTileRows);
+    if (m.pieces == 8) {
+      src_off = 3328 + 2 * si;
+    } else {
+      const int h = lane_or_row >> 4;
+      const int src_lane = 16 * h + si;
+      if (m.pieces == 2) {
+        src_off = 3072 + 8 * src_lane;
+      } else if (q < 128) {
+        src_off = 512 * (q >> 5) + 16 * src_lane;
+      } else {
+        src_off = 2048 + 512 * ((q - 128) >> 5) + 16 * src_lane;
+      }
+    }
+    const uint8_t* src = P + ((src_row / kTileRows) * nb + b) * kTileBytes + src_off;
+    for (int k2 = 0; k2 < m.len; k2 += 2) {
+      const uint16_t v = *reinterpret_cast<const uint16_t*>(src + k2);
+      buf[p * m.len + k2] = (uint8_t)(v & 0xff);
+      buf[p * m.len + k2 + 1] = (uint8_t)(v >> 8);
+    }
+  }
+  *reinterpret_cast<uint4*>(out + t * kTileBytes + 16 * q) = *reinterpret_cast<const uint4*>(buf);
+}
+
+// Per-expert token lists (one CTA of 1024 threads): counting sort of the
+// routing slots by expert, stable in slot order.  Slot s = t*k + j.
+__global__ void __launch_bounds__(1024) route_groups_kernel(const int32_t* __restrict__ topk,
+                                                            int n_slots, int k, int n_experts,
+                                                            int32_t* __restrict__ expert_ids,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ act_index,
+                                                            int32_t* __restrict__ slot_of,
+                                                            int32_t* __restrict__ status) {
+  __shared__ int cnt[4096];
+  __shared__ int wsum[33];
+  const int tid = threadIdx.x;
+  grid_dependency_wait();
+  for (int e = tid; e < n_experts; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int s = tid; s < n_slots; s += blockDim.x) {
+    const int e = topk[s];
+    if (e >= 0 && e < n_experts) {
+      atomicAdd(&cnt[e], 1);
+    } else if (status) {
+      *status = MMVQ_ERR_ROUTING;
+    }
+  }
+  __syncthreads();
+  // exclusive scan: thread tid owns experts [4tid, 4tid+4)
+  int local[4];
+  int sum = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int e = 4 * tid + u;
+    local[u] = e < n_experts ? cnt[e] : 0;
+    sum += local[u];
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  int x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += v;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int v = wsum[w];
+      wsum[w] = run;
+      run += v;
+    }
+    wsum[32] = run;
+  }
+  __syncthreads();
+  int run = wsum[warp] + x - sum;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int e = 4 * tid + u;
+    if (e < n_experts) {
+      offsets[e] = run;
+      expert_ids[e] = e;
+      cnt[e] = run;  // becomes the placement cursor
+    }
+    run += local[u];
+  }
+  if (tid == 0) offsets[n_experts] = wsum[32];
+  __syncthreads();
+  // stable placement by one warp, 32 slots at a time in slot order
+  if (warp == 0) {
+    for (int base = 0; base < n_slots; base += 32) {
+      const int s = base + lane;
+      int e = -1;
+      if (s < n_slots) {
+        const int v = topk[s];
+        if (v >= 0 && v < n_experts) e = v;
+      }
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      if (e >= 0) {
+        const int p = cnt[e] + rank;
+        act_index[p] = s / k;
+        slot_of[p] = s;
+      }
+      __syncwarp();
+      if (e >= 0 && rank == 0) cnt[e] += __popc(same);
+      __syncwarp();
+    }
+  }
+}
+
+int launch_repack_planar(const void* W, int64_t rows, int K, void* P, cudaStream_t s) {
+  const int nb = K / kQK;
+  const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * nb;
+  if (tiles > 0x7fffffff) return MMVQ_ERR_SHAPE;
+  repack_planar_kernel<<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint8_t*>(W), rows, nb,
+                                                       static_cast<uint8_t*>(P));
+  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+}
+
+int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_ids, int n,
+                         void* out, int32_t* status, cudaStream_t s) {
+  const int nb = K / kQK;
+  const int64_t tiles = ((int64_t)(n + kTileRows - 1) / kTileRows) * nb;
+  if (tiles > 0x7fffffff) return MMVQ_ERR_SHAPE;
+  gather_planar_kernel<<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint8_t*>(P), rows, nb,
+                                                       row_ids, n, static_cast<uint8_t*>(out),
+                                                       status);
+  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+}
+
+int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                        int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
+                        cudaStream_t s) {
+  route_groups_kernel<<<1, 1024, 0, s>>>(topk, T * k, k, n_experts, expert_ids, offsets, act_index,
+                                         slot_of, status);
+  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+}
+
+}  // namespace mmvq

@@ -1,0 +1,214 @@
+"""Thin Python binding of libmmvq.so (include/mmvq.h).
+
+Argument marshalling only: every step of the path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors; each call runs on the current
+torch stream (or the one passed in).  If the library is missing the first
+call raises; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmmvq.so")
+
+TYPE_Q4_K = 12
+TYPE_Q6_K = 14
+TYPE_Q6_K_PLANAR = 1014
+BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210, TYPE_Q6_K_PLANAR: 210}
+Q8_1_BYTES = 36
+MAX_COLS = 8
+
+OK = 0
+ERR_TYPE, ERR_SHAPE, ERR_NCOLS, ERR_NULL, ERR_ALIGN, ERR_ROUTING, ERR_CUDA = -1, -2, -3, -4, -5, -6, -7
+
+# name -> (restype, argtypes); mirrors include/mmvq.h
+_P, _I, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+SIGNATURES = {
+    "mmvq_version": (_I, []),
+    "mmvq_strerror": (ctypes.c_char_p, [_I]),
+    "mmvq_quantize_q8_1": (_I, [_P, _I, _I, _I64, _P, _P]),
+    "mmvq_gemv": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P]),
+    "mmvq_debug_block_sums": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P, _P]),
+    "mmvq_grouped": (_I, [_I, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P]),
+    "mmvq_route_groups": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "mmvq_silu_mul_quantize_q8_1": (_I, [_P, _I, _I, _P, _P, _P]),
+    "mmvq_planar_bytes": (_I64, [_I64, _I]),
+    "mmvq_repack_planar": (_I, [_I, _P, _I64, _I, _P, _P]),
+    "mmvq_gather_planar_rows": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P]),
+}
+
+
+class MMVQError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (code {code})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m block_quantized_matvec_gb300.build` (nvcc, sm_103a)")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(l, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = l
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().mmvq_strerror(code).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise MMVQError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------- entry points --
+
+def quantize_q8_1(x: torch.Tensor, K: int | None = None, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """fp32 x [ncols, ldx] -> Q8_1 bytes [ncols, K/32, 36] (uint8)."""
+    _dev(x, "x")
+    if x.dtype != torch.float32:
+        raise ValueError("x must be float32")
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    ncols, ldx = x2.shape
+    K = ldx if K is None else K
+    if out is None:
+        out = torch.empty((ncols, K // 32, Q8_1_BYTES), dtype=torch.uint8, device=x.device)
+    _check(lib().mmvq_quantize_q8_1(_ptr(x2), K, ncols, ldx, _ptr(out), _stream(stream)),
+           "mmvq_quantize_q8_1")
+    return out
+
+
+def gemv(type_: int, W: torch.Tensor, rows: int, K: int, xq: torch.Tensor, ncols: int,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y [ncols, rows] fp32 = W (rows x K, block type ``type_``) times ncols Q8_1 columns."""
+    _dev(W, "W")
+    _dev(xq, "xq")
+    if out is None:
+        out = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
+    _check(lib().mmvq_gemv(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(out), _stream(stream)),
+           "mmvq_gemv")
+    return out
+
+
+def debug_block_sums(type_: int, W: torch.Tensor, rows: int, K: int, xq: torch.Tensor, ncols: int,
+                     stream=None):
+    """(sumi [ncols, rows, K/32] int32, y [ncols, rows]) from the gemv kernel itself."""
+    _dev(W, "W")
+    _dev(xq, "xq")
+    sumi = torch.empty((ncols, rows, K // 32), dtype=torch.int32, device=W.device)
+    y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
+    _check(lib().mmvq_debug_block_sums(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(sumi),
+                                       _ptr(y), _stream(stream)), "mmvq_debug_block_sums")
+    return sumi, y
+
+
+def grouped(type_: int, W_experts: torch.Tensor, n_experts: int, rows: int, K: int,
+            expert_ids: torch.Tensor, offsets: torch.Tensor, act_index: torch.Tensor | None,
+            xq: torch.Tensor, n_xq_cols: int, n_positions: int, out: torch.Tensor | None = None,
+            status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y [n_positions, rows]: row p = expert of p's group times xq column act_index[p]."""
+    for t, n in ((W_experts, "W_experts"), (expert_ids, "expert_ids"), (offsets, "offsets"),
+                 (xq, "xq")):
+        _dev(t, n)
+    if out is None:
+        out = torch.empty((max(n_positions, 1), rows), dtype=torch.float32, device=xq.device)
+    _check(lib().mmvq_grouped(type_, _ptr(W_experts), n_experts, rows, K, _ptr(expert_ids),
+                              _ptr(offsets), expert_ids.numel(), _ptr(act_index), _ptr(xq),
+                              n_xq_cols, _ptr(out), _ptr(status), _stream(stream)), "mmvq_grouped")
+    return out
+
+
+def route_groups(topk: torch.Tensor, n_experts: int, stream=None):
+    """topk [T, k] int32 -> (expert_ids [E], offsets [E+1], act_index [T*k], slot_of [T*k], status)."""
+    _dev(topk, "topk")
+    T, k = topk.shape
+    dev = topk.device
+    eids = torch.empty(n_experts, dtype=torch.int32, device=dev)
+    offs = torch.empty(n_experts + 1, dtype=torch.int32, device=dev)
+    act = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    slot = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().mmvq_route_groups(_ptr(topk) if T else None, T, k, n_experts, _ptr(eids),
+                                   _ptr(offs), _ptr(act), _ptr(slot), _ptr(status),
+                                   _stream(stream)), "mmvq_route_groups")
+    return eids, offs, act, slot, status
+
+
+def silu_mul_quantize_q8_1(gu: torch.Tensor, F: int, out: torch.Tensor | None = None,
+                           h_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gu [n, 2F] = [gate | up] -> Q8_1 of silu(gate)*up, [n, F/32, 36]."""
+    _dev(gu, "gu")
+    n = gu.shape[0]
+    if out is None:
+        out = torch.empty((n, F // 32, Q8_1_BYTES), dtype=torch.uint8, device=gu.device)
+    _check(lib().mmvq_silu_mul_quantize_q8_1(_ptr(gu), F, n, _ptr(out), _ptr(h_out),
+                                             _stream(stream)), "mmvq_silu_mul_quantize_q8_1")
+    return out
+
+
+def planar_bytes(rows: int, K: int) -> int:
+    n = lib().mmvq_planar_bytes(rows, K)
+    if n < 0:
+        raise MMVQError(ERR_SHAPE, "mmvq_planar_bytes")
+    return int(n)
+
+
+def repack_planar(W_gguf: torch.Tensor, rows: int, K: int, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """GGUF Q6_K bytes -> planar tiles (uint8, planar_bytes(rows, K))."""
+    _dev(W_gguf, "W_gguf")
+    if out is None:
+        out = torch.empty(planar_bytes(rows, K), dtype=torch.uint8, device=W_gguf.device)
+    _check(lib().mmvq_repack_planar(TYPE_Q6_K, _ptr(W_gguf), rows, K, _ptr(out), _stream(stream)),
+           "mmvq_repack_planar")
+    return out
+
+
+def gather_planar_rows(W_planar: torch.Tensor, rows: int, K: int, row_ids: torch.Tensor,
+                       out: torch.Tensor | None = None, stream=None):
+    """Planar matrix of len(row_ids) rows, row k = row row_ids[k] of W_planar; returns (out, status)."""
+    _dev(W_planar, "W_planar")
+    _dev(row_ids, "row_ids")
+    n = row_ids.numel()
+    if out is None:
+        out = torch.empty(planar_bytes(n, K), dtype=torch.uint8, device=W_planar.device)
+    status = torch.zeros(1, dtype=torch.int32, device=W_planar.device)
+    _check(lib().mmvq_gather_planar_rows(_ptr(W_planar), rows, K, _ptr(row_ids), n, _ptr(out),
+                                         _ptr(status), _stream(stream)), "mmvq_gather_planar_rows")
+    return out, status

@@ -1,0 +1,198 @@
+/*
+ * mmvq.h: C ABI of libmmvq.so, block-quantized weight x Q8_1 activation
+ * matrix-vector products (MMVQ) at 1-8 columns, for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named W, xq, x, y, gu, sumi, row_ids, topk, expert_ids,
+ *    token_offsets, act_index, status and out are DEVICE pointers, owned by
+ *    the caller, who allocates and frees them.  The library allocates no
+ *    device or host memory and never synchronises the stream.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  Launch failures are reported by the return
+ *    value; faults inside a kernel surface at the caller's next sync.
+ *  - Return value: MMVQ_OK (0) or a negative mmvq_status.  Arguments are
+ *    checked on the host before any CUDA call, so a rejected call launches
+ *    nothing and leaves every buffer untouched.
+ *  - Alignment: W, xq and out must be 16-byte aligned; x, y, gu and the
+ *    int32 arrays 4-byte aligned.
+ *  - There is no CPU fallback: without a usable sm_103a device a launch
+ *    fails with MMVQ_ERR_CUDA.
+ *
+ * Formats (the pages are the Strata engine's SYCL port: PRs #2746, #2340,
+ * #2207, #1774 and issue #2801; the byte arrangement inside each block is
+ * the GGUF one):
+ *  - Q8_1 block, 36 bytes per 32 activations: fp16 d, fp16 s, int8 q[32];
+ *    d = amax/127, q = round-half-away(x/d), s = d * sum(q) (PR #2340,
+ *    "int4 activation loads": quants 4-byte aligned behind the header).
+ *  - Q6_K block, 210 bytes per 256 weights: ql[128] low nibbles, qh[64]
+ *    2-bit high fields, int8 scales[16] (one per 16 weights), fp16 d.
+ *    Weight = d * scale * (q - 32), q in 0..63 (PR #2340, "Q6_K six-bit
+ *    offset as SWAR").
+ *  - Q4_K block, 144 bytes per 256 weights: fp16 d, fp16 dmin, 12 bytes of
+ *    packed 6-bit scales and mins for 8 sub-blocks of 32, qs[128] nibbles.
+ *    Weight = d * sc * q - dmin * m.
+ *  - Dense matrices are row-major: row r holds K/256 consecutive blocks.
+ *  - Planar Q6_K (MMVQ_Q6_K_PLANAR), this library's load-time layout after
+ *    PR #2340 "STRATA_Q6_PLANAR" (the same bytes, as ql/qh/scales/d planes,
+ *    so every load is an aligned 16-byte load).  Rows are taken in groups
+ *    of 16 (the last group padded with zero rows).  The matrix is a
+ *    sequence of 3360-byte tiles T(g, b), g = row group (major), b = 256-block
+ *    (minor).  Inside a tile, lane L = 16*h + i, where i = row in the group
+ *    and h = half of the block:
+ *      bytes [512*j + 16*L, +16)         j = 0..3 : ql[64*h + 16*j .. +15]
+ *      bytes [2048 + 512*j + 16*L, +16)  j = 0..1 : qh[32*h + 16*j .. +15]
+ *      bytes [3072 + 8*L, +8)                     : scales[8*h .. 8*h+7]
+ *      bytes [3328 + 2*i, +2)                     : d
+ *    so each warp-wide 16-byte load reads one contiguous 512-byte segment.
+ *    Size: mmvq_planar_bytes(rows, K).
+ *
+ * Results: y is fp32, [ncols][rows] (column-major over the activation
+ * columns).  Block sums are exact integers; the FP32 output of a row is
+ * sum over 32-blocks of d_w*d_a*sumi (Q4_K: minus dmin*m*s_a), summed in an
+ * order that differs from plain index order only in rounding (PR #1774,
+ * "What changed": only the sub-block summation order differs, so the last
+ * bits can differ).
+ */
+#ifndef MMVQ_H_
+#define MMVQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mmvq_stream_t; /* == cudaStream_t */
+
+/* Symbols of this ABI are the only ones the library exports. */
+#if defined(__GNUC__)
+#define MMVQ_API __attribute__((visibility("default")))
+#else
+#define MMVQ_API
+#endif
+
+enum mmvq_type {
+  MMVQ_Q4_K = 12,         /* GGUF Q4_K blocks, 144 B / 256 weights */
+  MMVQ_Q6_K = 14,         /* GGUF Q6_K blocks, 210 B / 256 weights */
+  MMVQ_Q6_K_PLANAR = 1014 /* Q6_K in 16-row planar tiles (see above) */
+};
+
+enum mmvq_status {
+  MMVQ_OK = 0,
+  MMVQ_ERR_TYPE = -1,    /* type not supported by this entry point */
+  MMVQ_ERR_SHAPE = -2,   /* K % 256 (K % 32 for Q8_1), rows/n <= 0, sizes too large */
+  MMVQ_ERR_NCOLS = -3,   /* ncols outside 1..8 */
+  MMVQ_ERR_NULL = -4,    /* a required pointer is NULL */
+  MMVQ_ERR_ALIGN = -5,   /* a pointer breaks its alignment rule */
+  MMVQ_ERR_ROUTING = -6, /* routing lists rejected (host-side limits) */
+  MMVQ_ERR_CUDA = -7     /* a CUDA launch or attribute call failed */
+};
+
+/* Version of this ABI (major*10000 + minor*100 + patch). */
+MMVQ_API int mmvq_version(void);
+
+/* Human-readable text for a status code (static storage). */
+MMVQ_API const char* mmvq_strerror(int code);
+
+/*
+ * Q8_1 activation quantisation (PR #2340 "int4 activation loads"; PR #1774
+ * "d * ds * sumi").  x: fp32 [ncols][ldx]; the first K values of each column
+ * are quantised in blocks of 32 into xq: [ncols][K/32] Q8_1 blocks (36 B).
+ * Bit-exact: d = fp16(amax/127), q = roundf(x/d) (0 when amax = 0),
+ * s = fp16(d*sum q) with d unrounded; fp16 conversions round to nearest even.
+ * Requires K % 32 == 0, K > 0, ldx >= K, 1 <= ncols <= 65535.
+ */
+MMVQ_API int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq,
+                       mmvq_stream_t stream);
+
+/*
+ * Dense MMVQ (PR #2207 wide kernels, PR #1774 iq3s_wide_kernel: weights read
+ * once for all 1-8 columns).  W: rows x K/256 blocks of `type` (MMVQ_Q4_K,
+ * MMVQ_Q6_K or MMVQ_Q6_K_PLANAR); xq: [ncols][K/32] Q8_1 blocks;
+ * y: fp32 [ncols][rows].  Requires K % 256 == 0 (PR #1774: the row length a
+ * multiple of 256), 1 <= ncols <= 8 (PR #2207: 1 to 8 columns),
+ * K <= 16384, 1 <= rows <= 2^31 - 1.
+ */
+MMVQ_API int mmvq_gemv(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
+              mmvq_stream_t stream);
+
+/*
+ * The per-32-block integer sums the dense product forms, for parity checks:
+ * sumi: int32 [ncols][rows][K/32], sumi = sc0*sum16 + sc1*sum16 (Q6_K) or
+ * sc*sum32 (Q4_K).  Runs the same kernel as mmvq_gemv (with y also written
+ * to `y` when y != NULL).  Same argument rules as mmvq_gemv.
+ */
+MMVQ_API int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
+                          int32_t* sumi, float* y, mmvq_stream_t stream);
+
+/*
+ * Grouped expert MMVQ over per-expert token lists (PR #2746 "B70
+ * validation": grouped calls with empty groups; issue #2801: the grouped
+ * gate/up and down kernels).  W_experts: [n_experts][rows][K/256] blocks of
+ * `type` (MMVQ_Q4_K or MMVQ_Q6_K).  Group g (0 <= g < n_groups) multiplies
+ * expert expert_ids[g] with the activation columns of positions
+ * p in [token_offsets[g], token_offsets[g+1]); column act_index[p] of xq
+ * (column p when act_index == NULL).  Output row p: y[p][0..rows).
+ * xq: [n_xq_cols][K/32] Q8_1 blocks.  Empty groups are legal and cost
+ * nothing.  Groups may hold any number of positions (processed 8 at a time).
+ * Device-side checks: an expert id outside [0, n_experts), decreasing
+ * offsets or an activation index outside [0, n_xq_cols) skip that group or
+ * position and set *status to MMVQ_ERR_ROUTING when status != NULL (the
+ * caller clears *status beforehand).  Host limits: 1 <= n_groups <= 4096,
+ * K % 256 == 0, K <= 16384, rows >= 1, n_experts >= 1.
+ */
+MMVQ_API int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, int K,
+                 const int32_t* expert_ids, const int32_t* token_offsets, int n_groups,
+                 const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
+                 int32_t* status, mmvq_stream_t stream);
+
+/*
+ * Per-expert token lists from top-k routing: all n_experts groups in id order
+ * (expert_ids[e] = e, token_offsets [n_experts+1]), positions inside a group
+ * in token order; act_index[p] = token of position p, slot_of[p] = t*k + j
+ * for routing entry topk[t][j].  topk: int32 [T][k].  Out-of-range expert ids
+ * are dropped and set *status to MMVQ_ERR_ROUTING when status != NULL.
+ * Requires 1 <= n_experts <= 4096, T >= 0, 1 <= k, T*k <= 65536.
+ */
+MMVQ_API int mmvq_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                      int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
+                      int32_t* status, mmvq_stream_t stream);
+
+/*
+ * SiLU(gate) * up, requantised to Q8_1 between the grouped gate/up and down
+ * calls.  gu: fp32 [n][2F] rows laid out [gate F | up F] (the grouped
+ * gate/up output when the expert's first F rows are gate and the next F
+ * rows up).  h = gate/(1+exp(-gate)) * up in fp32, then Q8_1 as
+ * mmvq_quantize_q8_1 into xq: [n][F/32].  h_out (may be NULL): fp32 [n][F].
+ * Requires F % 32 == 0, F > 0, n >= 1.
+ */
+MMVQ_API int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq, float* h_out,
+                                mmvq_stream_t stream);
+
+/* Bytes of the planar Q6_K form of a rows x K matrix; -1 on bad shape. */
+MMVQ_API int64_t mmvq_planar_bytes(int64_t rows, int K);
+
+/*
+ * Load-time repack of GGUF Q6_K blocks into planar tiles (PR #2340
+ * "STRATA_Q6_PLANAR": same bytes, the GGUF copy can then be freed).
+ * Out-of-place; W_planar holds mmvq_planar_bytes(rows, K) bytes; pad rows
+ * are written as zeros.  type must be MMVQ_Q6_K.  K % 256 == 0.
+ */
+MMVQ_API int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int K, void* W_planar,
+                       mmvq_stream_t stream);
+
+/*
+ * Draft-head gather (PR #2340: "the draft head's subset is gathered from the
+ * planar head"): out = planar matrix of n rows whose row k is row
+ * row_ids[k] of the planar matrix W_planar (rows x K).  out holds
+ * mmvq_planar_bytes(n, K) bytes.  Row ids outside [0, rows) give zero rows
+ * and set *status to MMVQ_ERR_ROUTING when status != NULL.
+ */
+MMVQ_API int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int32_t* row_ids,
+                            int n, void* out, int32_t* status, mmvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MMVQ_H_ */

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads without a GPU, exports exactly the entry
+points include/mmvq.h declares, and rejects bad arguments on the host
+before any CUDA call (so these run on a machine with no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_quantized_matvec_gb300 import build, mmvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return mmvq.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "mmvq.h")).read()
+    return set(re.findall(r"MMVQ_API\s+[\w\s\*]+?\b(mmvq_\w+)\s*\(", text))
+
+
+def test_header_declares_the_binding_signatures():
+    assert _declared() == set(mmvq.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {mmvq.LIB_PATH}").read().split("\n")
+    exported = {l.split()[-1] for l in out if l.strip() and l.split()[-1].startswith("mmvq_")}
+    assert exported == _declared()
+
+
+def test_version_and_strerror(lib):
+    assert lib.mmvq_version() == 10000
+    for code in range(0, -8, -1):
+        assert mmvq.strerror(code) and "unknown" not in mmvq.strerror(code)
+    assert "unknown" in mmvq.strerror(-99)
+
+
+def test_planar_bytes_host_only(lib):
+    assert mmvq.planar_bytes(151936, 2560) == 151936 // 16 * 10 * 3360 == 151936 * 10 * 210
+    assert mmvq.planar_bytes(17, 256) == 2 * 1 * 3360
+    assert lib.mmvq_planar_bytes(16, 100) == -1
+    assert lib.mmvq_planar_bytes(0, 256) == -1
+
+
+A = 0x10000  # an aligned fake device address: never dereferenced, calls fail before CUDA
+
+
+@pytest.mark.parametrize("args,code", [
+    ((99, A, 16, 256, A, 1, A, None), mmvq.ERR_TYPE),
+    ((14, A, 16, 255, A, 1, A, None), mmvq.ERR_SHAPE),
+    ((14, A, 16, 128, A, 1, A, None), mmvq.ERR_SHAPE),
+    ((14, A, 16, 16384 + 256, A, 1, A, None), mmvq.ERR_SHAPE),
+    ((14, A, 0, 256, A, 1, A, None), mmvq.ERR_SHAPE),
+    ((14, A, 16, 256, A, 0, A, None), mmvq.ERR_NCOLS),
+    ((14, A, 16, 256, A, 9, A, None), mmvq.ERR_NCOLS),
+    ((14, None, 16, 256, A, 1, A, None), mmvq.ERR_NULL),
+    ((14, A, 16, 256, None, 1, A, None), mmvq.ERR_NULL),
+    ((14, A, 16, 256, A, 1, None, None), mmvq.ERR_NULL),
+    ((14, A + 8, 16, 256, A, 1, A, None), mmvq.ERR_ALIGN),
+    ((1014, A, 16, 256, A + 4, 1, A, None), mmvq.ERR_ALIGN),
+    ((12, A, 16, 256, A, 1, A + 2, None), mmvq.ERR_ALIGN),
+])
+def test_gemv_rejects_bad_arguments_on_host(lib, args, code):
+    assert lib.mmvq_gemv(*args) == code
+
+
+def test_other_entry_points_reject_bad_arguments_on_host(lib):
+    L = lib
+    assert L.mmvq_quantize_q8_1(A, 48, 1, 48, A, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_quantize_q8_1(A, 64, 1, 32, A, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_quantize_q8_1(None, 64, 1, 64, A, None) == mmvq.ERR_NULL
+    assert L.mmvq_quantize_q8_1(A, 64, 1, 64, A + 4, None) == mmvq.ERR_ALIGN
+    assert L.mmvq_quantize_q8_1(A, 64, 0, 64, A, None) == mmvq.ERR_SHAPE
+    g = (12, A, 256, 1536, 2560, A, A, 256, A, A, 1, A, None, None)
+    assert L.mmvq_grouped(*g[:0], 14 + 1000, *g[1:]) == mmvq.ERR_TYPE
+    assert L.mmvq_grouped(*g[:7], 0, *g[8:]) == mmvq.ERR_ROUTING
+    assert L.mmvq_grouped(*g[:7], 4097, *g[8:]) == mmvq.ERR_ROUTING
+    assert L.mmvq_grouped(*g[:4], 2560 + 32, *g[5:]) == mmvq.ERR_SHAPE
+    assert L.mmvq_grouped(*g[:5], None, *g[6:]) == mmvq.ERR_NULL
+    assert L.mmvq_grouped(*g[:9], A + 4, *g[10:]) == mmvq.ERR_ALIGN
+    assert L.mmvq_route_groups(A, 4, 8, 0, A, A, A, A, None, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_route_groups(A, 10000, 8, 256, A, A, A, A, None, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_route_groups(None, 4, 8, 256, A, A, A, A, None, None) == mmvq.ERR_NULL
+    assert L.mmvq_silu_mul_quantize_q8_1(A, 768 + 16, 1, A, None, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_silu_mul_quantize_q8_1(A, 768, 0, A, None, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_repack_planar(12, A, 16, 256, A, None) == mmvq.ERR_TYPE
+    assert L.mmvq_repack_planar(14, A, 16, 256, A + 8, None) == mmvq.ERR_ALIGN
+    assert L.mmvq_gather_planar_rows(A, 16, 256, A, 0, A, None, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_gather_planar_rows(A, 16, 256, A, 4, A + 8, None, None) == mmvq.ERR_ALIGN
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "block_quantized_matvec_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "mmvq_oracle" not in text, f
