@@ -6,15 +6,16 @@ Default workload: the Q6_K sweep -- 2560x2560, 2560x10240 and 10240x2560
 planar tiles -- the pages' mmvq_bench table ("Strata" PR #2207).  One step
 is one pass over every (shape, columns) case on every resident copy of its
 matrix; the copies of each shape total more than twice the L2 size, so no
-call finds its weights in L2.  Each call is the hot path: Q8_1 quantisation
-of the fp32 columns, then the MMVQ kernel.
+call finds its weights in L2.  Per case the hot path runs as in decode: the
+fp32 columns are quantised to Q8_1 once, then every matrix copy gets its
+MMVQ call (several matrices sharing one activation, like q/k/v or gate/up).
 
 The step's calls are made through the public binding and captured once as a
-CUDA graph (the pages' figures are graph replays too, PR #2746), with an
-event-record node around every kernel, so every kernel's duration comes
-from the timed region itself.  `value` = weight bytes of all calls / device
-time; `e2e` repeats the step with the fp32 columns copied in from pinned
-host memory and all outputs read back every step.
+CUDA graph (the pages' figures are graph replays too, PR #2746), with
+event-record nodes at the boundaries of each case, so each case's MMVQ time
+comes from the timed region itself.  `value` = weight bytes of all calls /
+device time of the step; `e2e` repeats the step with the fp32 columns copied
+in from pinned host memory and all outputs read back every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a row sample
@@ -108,6 +109,15 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first_sample(self, timeout_s: float = 10.0):
+        """nvidia-smi's start-up can stall the GPU: let it settle before timing."""
+        t = time.time()
+        while self.proc is not None and len(self.lines) < 2 and time.time() - t < timeout_s:
+            time.sleep(0.02)
+
+    def mark(self):
+        self.first_timed = len(self.lines)
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -119,7 +129,8 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        timed = self.lines[getattr(self, "first_timed", 0):] or self.lines[-1:]
+        for l in timed:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -181,7 +192,7 @@ def run_ours(args, rank, world, local_rank):
         if fmt == "q6_k_planar":
             Wd = mmvq.repack_planar(Wd, rows, K)
         nbytes = metrics.weight_bytes(fmt, rows, K)
-        copies = max(2, math.ceil(2 * l2 / nbytes)) if not args.no_rotate else 1
+        copies = max(2, math.ceil(2 * l2 / nbytes))
         mats.append([Wd] + [Wd.clone() for _ in range(copies - 1)])
     torch.cuda.synchronize()
 
@@ -207,22 +218,31 @@ def run_ours(args, rank, world, local_rank):
             y_total += nc * rows
     y_dev = torch.empty(y_total, dtype=torch.float32, device=dev)
     y_pinned = torch.empty(y_total, dtype=torch.float32).pin_memory()
+    calls_of_case = [[i for i, c in enumerate(calls) if c[0] == ci] for ci in range(len(case_list))]
 
-    def call(i, stream=None):
-        ci, cp, yo = calls[i]
+    def run_case(ci, s=None, evs=None):
+        """Quantise the case's columns once, then every copy's MMVQ back to back."""
         si, fmt, rows, K, nc, xo = case_list[ci]
-        x = x_dev[xo:xo + nc * K].view(nc, K)
-        mmvq.quantize_q8_1(x, out=xq_bufs[ci])
-        mmvq.gemv(type_of[fmt], mats[si][cp], rows, K, xq_bufs[ci], nc,
-                  out=y_dev[yo:yo + nc * rows].view(nc, rows))
+        if evs is not None:
+            _record_external(evs[3 * ci], s)
+        mmvq.quantize_q8_1(x_dev[xo:xo + nc * K].view(nc, K), out=xq_bufs[ci])
+        if evs is not None:
+            _record_external(evs[3 * ci + 1], s)
+        for i in calls_of_case[ci]:
+            _, cp, yo = calls[i]
+            mmvq.gemv(type_of[fmt], mats[si][cp], rows, K, xq_bufs[ci], nc,
+                      out=y_dev[yo:yo + nc * rows].view(nc, rows))
+        if evs is not None:
+            _record_external(evs[3 * ci + 2], s)
 
-    # first calls outside any capture (kernel attributes, occupancy)
-    for i in range(len(calls)):
-        call(i)
+    # first calls outside any capture (kernel attributes, launch shapes)
+    for ci in range(len(case_list)):
+        run_case(ci)
     torch.cuda.synchronize()
 
-    # capture the step with an event node before each kernel and after the last
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(calls) + 1)]
+    # the step as one CUDA graph; event nodes at the case boundaries only, so
+    # consecutive MMVQ launches stay chained by programmatic dependent launch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 * len(case_list))]
     for e in evs:
         e.record()
     torch.cuda.synchronize()
@@ -231,32 +251,29 @@ def run_ours(args, rank, world, local_rank):
     cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
         s = torch.cuda.current_stream()
-        for i in range(len(calls)):
-            ci, cp, yo = calls[i]
-            si, fmt, rows, K, nc, xo = case_list[ci]
-            _record_external(evs[2 * i], s)
-            mmvq.quantize_q8_1(x_dev[xo:xo + nc * K].view(nc, K), out=xq_bufs[ci])
-            _record_external(evs[2 * i + 1], s)
-            mmvq.gemv(type_of[fmt], mats[si][cp], rows, K, xq_bufs[ci], nc,
-                      out=y_dev[yo:yo + nc * rows].view(nc, rows))
-        _record_external(evs[-1], s)
+        for ci in range(len(case_list)):
+            run_case(ci, s, evs)
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
+    import torch.distributed as dist
+    gpu_index = local_rank
+    if "CUDA_VISIBLE_DEVICES" in os.environ:
+        vis = os.environ["CUDA_VISIBLE_DEVICES"].split(",")
+        if local_rank < len(vis) and vis[local_rank].strip().isdigit():
+            gpu_index = int(vis[local_rank])
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
-
-    import torch.distributed as dist
+    clocks.wait_first_sample()
     if world > 1:
         dist.barrier()
-    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
-    clocks.start()
-    time.sleep(0.3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    clocks.mark()
     t0.record(stream)
     for _ in range(args.steps):
         graph.replay()
@@ -270,24 +287,23 @@ def run_ours(args, rank, world, local_rank):
         elapsed_ms = float(tt.item())
         dist.barrier()
 
-    # per-kernel durations from the event nodes of the last step
-    q_us = np.array([evs[2 * i].elapsed_time(evs[2 * i + 1]) * 1e3 for i in range(len(calls))])
-    g_us = np.array([evs[2 * i + 1].elapsed_time(evs[2 * i + 2]) * 1e3 for i in range(len(calls))])
+    # per-case durations from the event nodes of the last step
+    q_us = np.array([evs[3 * ci].elapsed_time(evs[3 * ci + 1]) * 1e3 for ci in range(len(case_list))])
+    g_us = np.array([evs[3 * ci + 1].elapsed_time(evs[3 * ci + 2]) * 1e3
+                     for ci in range(len(case_list))])
 
     peak, peak_kind = load_peak()
     w_step = 0
     alg_step = 0
     per_case = []
     for ci, (si, fmt, rows, K, nc, xo) in enumerate(case_list):
-        idx = [i for i, c in enumerate(calls) if c[0] == ci]
+        n = len(calls_of_case[ci])
         wb = metrics.weight_bytes(fmt, rows, K)
-        ab = metrics.call_bytes(fmt, rows, K, nc)
-        w_step += wb * len(idx)
-        alg_step += ab * len(idx)
-        gu = float(np.mean(g_us[idx]))
-        qu = float(np.mean(q_us[idx]))
-        per_case.append({"shape": f"{rows}x{K}", "fmt": fmt, "ncols": nc,
-                         "us_per_call": round(gu, 3), "us_quantize": round(qu, 3),
+        w_step += wb * n
+        alg_step += metrics.call_bytes(fmt, rows, K, nc) * n
+        gu = float(g_us[ci]) / n
+        per_case.append({"shape": f"{rows}x{K}", "fmt": fmt, "ncols": nc, "calls": n,
+                         "us_per_call": round(gu, 3), "us_quantize": round(float(q_us[ci]), 3),
                          "weight_gbps": round(wb / gu / 1e3, 1),
                          "frac_of_measured": round(wb / gu / 1e3 / peak, 3)})
     step_s = elapsed_ms / 1e3 / args.steps
@@ -317,16 +333,17 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": len(calls),
                    "weight_copies": [len(m) for m in mats],
                    "l2": "weights rotated over copies > 2x L2 per shape (inputs larger than L2)",
-                   "timing": "CUDA graph replay; event nodes around every kernel",
+                   "timing": "CUDA graph replay of the step; event nodes at case boundaries",
+                   "step": "per case: Q8_1-quantise its columns once, then one MMVQ per weight copy",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": None,
                      "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": "mmvq_dense_kernel (all launches of the step)"},
+                     "kernel": "mmvq_dense_kernel (all MMVQ launches of the last timed step)"},
         "e2e": {"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
                 "steps": e2e_steps},
-        "gpu_launches": 2 * len(calls) * args.steps,
+        "gpu_launches": (len(calls) + len(case_list)) * args.steps,
         "clocks": clk,
         "cases": per_case,
     }
@@ -408,6 +425,27 @@ def run_reference(args, rank, world):
     }
 
 
+def run_case_for_profile(spec: str, launches: int):
+    """One case, launched `launches` times eagerly (for ncu -k/-s/-c captures).
+    spec = fmt:ROWSxK:NCOLS, e.g. q6_k_planar:2560x10240:8."""
+    import torch
+    from block_quantized_matvec_gb300 import mmvq, synth
+    fmt, shape, nc = spec.split(":")
+    rows, K = (int(v) for v in shape.split("x"))
+    nc = int(nc)
+    t = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K}[fmt]
+    gen = synth.q4_k_weights if fmt == "q4_k" else synth.q6_k_weights
+    W = torch.from_numpy(gen(rows, K).reshape(-1)).cuda()
+    if fmt == "q6_k_planar":
+        W = mmvq.repack_planar(W, rows, K)
+    xq = mmvq.quantize_q8_1(torch.from_numpy(synth.activations(K, nc)).cuda())
+    y = torch.empty((nc, rows), device="cuda")
+    for _ in range(launches):
+        mmvq.gemv(t, W, rows, K, xq, nc, out=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"case": spec, "launches": launches, "y0": float(y[0, 0])}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,10 +455,16 @@ def main():
     ap.add_argument("--workload", default="q6k_sweep", choices=sorted(WORKLOAD_DESC))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-rotate", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--case", default=None,
+                    help="profile mode: launch one case (fmt:ROWSxK:NCOLS) --launches times")
+    ap.add_argument("--launches", type=int, default=8)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+
+    if args.case:
+        run_case_for_profile(args.case, args.launches)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

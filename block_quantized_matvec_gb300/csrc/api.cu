@@ -17,6 +17,7 @@ int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,
 int launch_repack_planar(const void* W, int64_t rows, int K, void* P, cudaStream_t s);
 int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_ids, int n,
                          void* out, int32_t* status, cudaStream_t s);
+int read_device_fault(int* fault, cudaStream_t stream);
 int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
                         int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
                         cudaStream_t s);
@@ -154,6 +155,11 @@ int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int
     return MMVQ_ERR_ALIGN;
   return mmvq::launch_gather_planar(W_planar, rows, K, row_ids, n, out, status,
                                     (cudaStream_t)stream);
+}
+
+int mmvq_read_device_fault(int* fault, mmvq_stream_t stream) {
+  if (!fault) return MMVQ_ERR_NULL;
+  return mmvq::read_device_fault(fault, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -69,30 +69,78 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;");
 }
 
+// Prefetch [p, p + bytes) into L2 (bulk, asynchronous, no completion to
+// wait for).  p is rounded down and the size up to 16 bytes; the caller
+// keeps the range inside its allocation.  Safe before griddepcontrol.wait:
+// L2 is the point of coherence, so data written afterwards by the preceding
+// kernel still wins, and nothing is held in L1 or registers.
+__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15);
+  int64_t n = (int64_t)(reinterpret_cast<uintptr_t>(p) + bytes - a);
+  n &= ~int64_t(15);
+  while (n > 0) {
+    const uint32_t chunk = (uint32_t)(n > (1 << 20) ? (1 << 20) : n);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(chunk) : "memory");
+    n -= chunk;
+    a += chunk;
+  }
+}
+
 // Stage Q8_1 columns into shared memory: quants into the padded byte rows,
 // d (and s when wanted) as floats.  act: [ncols][act_row_bytes(K)] bytes,
-// da/sa: [ncols][K/32].  col_of(c) gives the xq column for local column c.
+// da/sa: [ncols][K/32].  col_of(c) gives the xq column for local column c,
+// or -1 for a column to stage as zeros.  A column's blocks are one
+// contiguous, 16-byte aligned run of 36*K/32 bytes (K % 256 == 0), read
+// here 16 bytes per thread and scattered word by word.
 template <typename ColOf>
 __device__ __forceinline__ void stage_q8_1(const uint8_t* __restrict__ xq, int K, int ncols,
                                            ColOf col_of, uint8_t* act, float* da, float* sa,
                                            int tid, int nthreads) {
   const int nbq = K / kQK8;
-  const int total = ncols * nbq * 9;  // 9 words per block: header + 8 quant words
+  const int vec_per_col = nbq * 9 / 4;  // 16-byte vectors per column
+  const int total = ncols * vec_per_col;
   const int rb = act_row_bytes(K);
-  for (int w = tid; w < total; w += nthreads) {
-    const int c = w / (nbq * 9);
-    const int rem = w - c * nbq * 9;
-    const int kb = rem / 9;
-    const int k = rem - kb * 9;
-    const uint8_t* blk = xq + ((size_t)col_of(c) * nbq + kb) * kQ81Bytes;
-    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(blk) + k);
-    if (k == 0) {
-      da[c * nbq + kb] = half_bits_to_float((uint16_t)(v & 0xffff));
-      if (sa) sa[c * nbq + kb] = half_bits_to_float((uint16_t)(v >> 16));
-    } else {
-      *reinterpret_cast<uint32_t*>(act + c * rb + act_off(kb) + 4 * (k - 1)) = v;
+  for (int v = tid; v < total; v += nthreads) {
+    const int c = v / vec_per_col;
+    const int vi = v - c * vec_per_col;
+    const int col = col_of(c);
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (col >= 0)
+      q = __ldg(reinterpret_cast<const uint4*>(xq + (size_t)col * nbq * kQ81Bytes) + vi);
+    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int w = 4 * vi + e;  // word index in the column
+      const int kb = w / 9;
+      const int k = w - kb * 9;
+      if (k == 0) {
+        da[c * nbq + kb] = half_bits_to_float((uint16_t)(w4[e] & 0xffff));
+        if (sa) sa[c * nbq + kb] = half_bits_to_float((uint16_t)(w4[e] >> 16));
+      } else {
+        *reinterpret_cast<uint32_t*>(act + c * rb + act_off(kb) + 4 * (k - 1)) = w4[e];
+      }
     }
   }
+}
+
+// Launches `kern` with programmatic stream serialization allowed, so that
+// it may start while the preceding kernel in the stream drains; every kernel
+// of this library waits (griddepcontrol.wait) before it reads anything the
+// preceding kernel may write, and lets its own dependents launch early.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
 }
 
 }  // namespace mmvq

@@ -10,12 +10,37 @@
 // streams its blocks with 16-byte loads, decodes in registers and
 // accumulates with dp4a; the K-slices are summed through shared memory in
 // a fixed order, so results are run-to-run deterministic.
+//
+// Latency: the launch lets the next kernel in the stream start early
+// (programmatic dependent launch), and before waiting for the preceding
+// kernel each CTA asks L2 for the weight bytes of its first row groups, so
+// the weight stream overlaps the previous kernel's tail and the activation
+// staging.  The host picks the K-split so that all row groups of small and
+// mid-size matrices are resident in one wave; large ones run persistently
+// and prefetch the next row group into L2 while computing the current one.
 #include <algorithm>
 #include <mutex>
+#include <unordered_map>
 
 #include "rowgroup.cuh"
 
 namespace mmvq {
+
+// Byte range of the weights of row group rg (16 rows, all K).
+template <int LAYOUT>
+__device__ __forceinline__ void rowgroup_range(const uint8_t* W, int64_t rows, int nb, int64_t rg,
+                                               const uint8_t** p, int64_t* bytes) {
+  if (LAYOUT == kQ6Planar) {
+    *p = W + rg * nb * kTileBytes;
+    *bytes = (int64_t)nb * kTileBytes;
+  } else {
+    const int bb = (LAYOUT == kQ4Gguf) ? kQ4KBytes : kQ6KBytes;
+    const int64_t r0 = rg * kTileRows;
+    const int64_t r1 = min(r0 + kTileRows, rows);
+    *p = W + r0 * nb * bb;
+    *bytes = (r1 - r0) * nb * bb;
+  }
+}
 
 template <int LAYOUT, int NCOLS>
 __global__ void __launch_bounds__(512) mmvq_dense_kernel(const uint8_t* __restrict__ W,
@@ -34,6 +59,7 @@ __global__ void __launch_bounds__(512) mmvq_dense_kernel(const uint8_t* __restri
   const int nbq = K / kQK8;
   const int rb = act_row_bytes(K);
   const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
+  const int64_t rg_stride = (int64_t)gridDim.x * WR;
 
   uint8_t* act = smem;
   float* da = reinterpret_cast<float*>(smem + NCOLS * rb);
@@ -42,14 +68,30 @@ __global__ void __launch_bounds__(512) mmvq_dense_kernel(const uint8_t* __restri
   uint8_t* stage =
       reinterpret_cast<uint8_t*>(red + nwarps * kMaxCols * kTileRows) + (size_t)warp * 2 * kGgufStage;
 
+  grid_launch_dependents();
+  if (wk == 0 && lane == 0) {
+    const int64_t rg = (int64_t)blockIdx.x * WR + wr;
+    if (rg < n_rg) {
+      const uint8_t* p;
+      int64_t bytes;
+      rowgroup_range<LAYOUT>(W, rows, nb, rg, &p, &bytes);
+      prefetch_l2(p, bytes);
+    }
+  }
   grid_dependency_wait();
   stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da, LAYOUT == kQ4Gguf ? sa : nullptr,
              tid, 32 * nwarps);
   __syncthreads();
 
-  for (int64_t rg0 = (int64_t)blockIdx.x * WR; rg0 < n_rg; rg0 += (int64_t)gridDim.x * WR) {
+  for (int64_t rg0 = (int64_t)blockIdx.x * WR; rg0 < n_rg; rg0 += rg_stride) {
     const int64_t rg = rg0 + wr;
     const int64_t row = rg * kTileRows + (lane & 15);
+    if (wk == 0 && lane == 0 && rg + rg_stride < n_rg) {  // next row group into L2
+      const uint8_t* p;
+      int64_t bytes;
+      rowgroup_range<LAYOUT>(W, rows, nb, rg + rg_stride, &p, &bytes);
+      prefetch_l2(p, bytes);
+    }
     float acc[NCOLS];
 #pragma unroll
     for (int c = 0; c < NCOLS; ++c) acc[c] = 0.0f;
@@ -109,48 +151,89 @@ int ensure_smem(const void* kern, size_t smem, size_t* smem_set, std::mutex* mu)
   return MMVQ_OK;
 }
 
+struct DenseCfg {
+  int wk, wr, grid;
+  size_t smem;
+};
+
+// Launch shape for a (rows, K) matrix, cached per shape:
+//  - many row groups (>= 8 per SM): one warp per row group, 8 per CTA,
+//    persistent grid of (CTAs resident per SM) x SMs;
+//  - otherwise the largest K-split WK (a divisor of K/256, at most 16 warps)
+//    that still keeps every row group's CTA resident in a single wave.
+template <int LAYOUT, int NCOLS>
+static int dense_config(int64_t rows, int K, DenseCfg* out) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, DenseCfg> cache;
+  static size_t smem_set = 48 * 1024;
+  const uint64_t key = ((uint64_t)rows << 8) | (uint64_t)(K / kQK);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return MMVQ_OK;
+    }
+  }
+  auto kern = mmvq_dense_kernel<LAYOUT, NCOLS>;
+  const int sms = device_sms();
+  const size_t limit = max_smem_optin();
+  if (sms <= 0 || limit == 0) return MMVQ_ERR_CUDA;
+  const int nb = K / kQK;
+  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
+
+  auto occupancy = [&](int nwarps, size_t smem, int* per_sm) -> int {
+    if (smem > limit) return MMVQ_ERR_SHAPE;
+    if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, 32 * nwarps, smem) !=
+        cudaSuccess)
+      return MMVQ_ERR_CUDA;
+    return MMVQ_OK;
+  };
+
+  DenseCfg cfg = {0, 0, 0, 0};
+  if (n_rg < (int64_t)sms * 8) {
+    for (int wk = std::min(nb, 16); wk >= 1; --wk) {
+      if (nb % wk) continue;
+      const size_t smem = mmvq_smem_bytes(LAYOUT, K, NCOLS, wk);
+      int per_sm = 0;
+      const int rc = occupancy(wk, smem, &per_sm);
+      if (rc == MMVQ_ERR_CUDA) return rc;
+      if (rc != MMVQ_OK || per_sm < 1) continue;
+      if (n_rg <= (int64_t)sms * per_sm) {
+        cfg = {wk, 1, (int)n_rg, smem};
+        break;
+      }
+    }
+  }
+  if (cfg.wk == 0) {
+    // persistent: 8 row groups per CTA iteration (fewer if shared memory is short)
+    for (int wr = 8; wr >= 1; --wr) {
+      const size_t smem = mmvq_smem_bytes(LAYOUT, K, NCOLS, wr);
+      int per_sm = 0;
+      const int rc = occupancy(wr, smem, &per_sm);
+      if (rc == MMVQ_ERR_CUDA) return rc;
+      if (rc != MMVQ_OK || per_sm < 1) continue;
+      const int64_t ctas = (n_rg + wr - 1) / wr;
+      cfg = {1, wr, (int)std::min<int64_t>(ctas, (int64_t)sms * per_sm), smem};
+      break;
+    }
+  }
+  if (cfg.wk == 0) return MMVQ_ERR_SHAPE;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = cfg;
+  *out = cfg;
+  return MMVQ_OK;
+}
+
 template <int LAYOUT, int NCOLS>
 static int launch_dense_t(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
                           int32_t* sumi, cudaStream_t stream) {
-  auto kern = mmvq_dense_kernel<LAYOUT, NCOLS>;
-  const int sms = device_sms();
-  if (sms <= 0) return MMVQ_ERR_CUDA;
-  const int nb = K / kQK;
-  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
-  // Enough warps in flight to cover HBM latency: about 16 per SM.  Small
-  // matrices split K across the warps of a CTA.
-  const int64_t want_warps = (int64_t)sms * 16;
-  int wk = 1;
-  if (n_rg < want_warps) {
-    const int64_t w = (want_warps + n_rg - 1) / n_rg;
-    wk = divisor_at_least(nb, (int)std::min<int64_t>(w, nb));
-    if (wk > 16) wk = 16;
-  }
-  int wr = std::max(1, 8 / wk);
-  if ((int64_t)wr > n_rg) wr = (int)n_rg;
-  int nwarps = wk * wr;
-  size_t smem = mmvq_smem_bytes(LAYOUT, K, NCOLS, nwarps);
-  const size_t limit = max_smem_optin();
-  while (smem > limit && nwarps > 1) {  // long rows x many columns: fewer warps
-    if (wr > 1) --wr; else wk = std::max(1, wk / 2);
-    nwarps = wk * wr;
-    smem = mmvq_smem_bytes(LAYOUT, K, NCOLS, nwarps);
-  }
-  if (smem > limit) return MMVQ_ERR_SHAPE;
-
-  static std::mutex mu;
-  static size_t smem_set = 48 * 1024;
-  if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * nwarps, smem) !=
-          cudaSuccess ||
-      per_sm <= 0)
-    return MMVQ_ERR_CUDA;
-  const int64_t ctas_needed = (n_rg + wr - 1) / wr;
-  const int grid = (int)std::min<int64_t>(ctas_needed, (int64_t)sms * per_sm);
-  dim3 block(32, wk, wr);
-  kern<<<grid, block, smem, stream>>>(W, rows, K, xq, y, sumi);
-  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+  DenseCfg cfg;
+  const int rc = dense_config<LAYOUT, NCOLS>(rows, K, &cfg);
+  if (rc != MMVQ_OK) return rc;
+  return launch_pdl(mmvq_dense_kernel<LAYOUT, NCOLS>, dim3(cfg.grid), dim3(32, cfg.wk, cfg.wr),
+                    cfg.smem, stream, W, rows, K, xq, y, sumi);
 }
 
 template <int LAYOUT>
@@ -169,12 +252,15 @@ static int launch_dense_layout(const uint8_t* W, int64_t rows, int K, const uint
   return MMVQ_ERR_NCOLS;
 }
 
+int launch_q6_planar_tma(const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
+                         int32_t* sumi, cudaStream_t s);
+
 int launch_dense(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
                  int32_t* sumi, cudaStream_t s) {
   const uint8_t* w = static_cast<const uint8_t*>(W);
   const uint8_t* x = static_cast<const uint8_t*>(xq);
   switch (type) {
-    case MMVQ_Q6_K_PLANAR: return launch_dense_layout<kQ6Planar>(w, rows, K, x, ncols, y, sumi, s);
+    case MMVQ_Q6_K_PLANAR: return launch_q6_planar_tma(W, rows, K, xq, ncols, y, sumi, s);
     case MMVQ_Q6_K: return launch_dense_layout<kQ6Gguf>(w, rows, K, x, ncols, y, sumi, s);
     case MMVQ_Q4_K: return launch_dense_layout<kQ4Gguf>(w, rows, K, x, ncols, y, sumi, s);
   }

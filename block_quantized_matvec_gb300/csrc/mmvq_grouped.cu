@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(512) mmvq_grouped_kernel(
   uint8_t* stage =
       reinterpret_cast<uint8_t*>(red + WK * kMaxCols * kTileRows) + (size_t)wk * 2 * kGgufStage;
 
+  grid_launch_dependents();
   grid_dependency_wait();
 
   // 1. compact the valid non-empty groups, in group order
@@ -142,23 +143,8 @@ __global__ void __launch_bounds__(512) mmvq_grouped_kernel(
         }
         __syncthreads();
         // an invalid column is staged as zeros (d = 0, q = 0): its rows come out 0
-        const int total = n * nbq * 9;
-        for (int w = tid; w < total; w += nthreads) {
-          const int c = w / (nbq * 9);
-          const int rem = w - c * nbq * 9;
-          const int kb = rem / 9;
-          const int k = rem - kb * 9;
-          const int col = cols_s[c];
-          uint32_t v = 0;
-          if (col >= 0)
-            v = __ldg(reinterpret_cast<const uint32_t*>(xq + ((size_t)col * nbq + kb) * kQ81Bytes) + k);
-          if (k == 0) {
-            da[c * nbq + kb] = half_bits_to_float((uint16_t)(v & 0xffff));
-            if (LAYOUT == kQ4Gguf) sa[c * nbq + kb] = half_bits_to_float((uint16_t)(v >> 16));
-          } else {
-            *reinterpret_cast<uint32_t*>(act + c * rb + act_off(kb) + 4 * (k - 1)) = v;
-          }
-        }
+        stage_q8_1(xq, K, n, [&](int c) { return cols_s[c]; }, act, da,
+                   LAYOUT == kQ4Gguf ? sa : nullptr, tid, nthreads);
         __syncthreads();
         staged_g = g;
         staged_p0 = p0;
@@ -208,10 +194,8 @@ static int launch_grouped_t(const uint8_t* W, int n_experts, int64_t rows, int K
   const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
   const int64_t max_items = (int64_t)n_groups * n_rg;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_items, (int64_t)sms * per_sm));
-  dim3 block(32, wk, 1);
-  kern<<<grid, block, smem, stream>>>(W, n_experts, rows, K, expert_ids, offsets, n_groups,
-                                      act_index, xq, n_xq_cols, y, status);
-  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+  return launch_pdl(kern, dim3(grid), dim3(32, wk, 1), smem, stream, W, n_experts, rows, K,
+                    expert_ids, offsets, n_groups, act_index, xq, n_xq_cols, y, status);
 }
 
 int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,

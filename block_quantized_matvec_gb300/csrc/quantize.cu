@@ -46,6 +46,7 @@ __device__ __forceinline__ void quantize_lane(float v, uint8_t* out, int lane) {
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int K,
                                                             int ncols, int64_t ldx,
                                                             uint8_t* __restrict__ xq) {
+  grid_launch_dependents();
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int nbq = K / kQK8;
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
 __global__ void __launch_bounds__(256) silu_mul_quantize_kernel(const float* __restrict__ gu, int F,
                                                                 int n, uint8_t* __restrict__ xq,
                                                                 float* __restrict__ h_out) {
+  grid_launch_dependents();
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int nbq = F / kQK8;
@@ -81,16 +83,16 @@ int launch_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq
                          cudaStream_t stream) {
   const int64_t blocks = (int64_t)ncols * (K / kQK8);
   const int grid = (int)((blocks + 7) / 8);
-  quantize_q8_1_kernel<<<grid, 256, 0, stream>>>(x, K, ncols, ldx, static_cast<uint8_t*>(xq));
-  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+  return launch_pdl(quantize_q8_1_kernel, dim3(grid), dim3(256), 0, stream, x, K, ncols, ldx,
+                    static_cast<uint8_t*>(xq));
 }
 
 int launch_silu_mul_quantize(const float* gu, int F, int n, void* xq, float* h_out,
                              cudaStream_t stream) {
   const int64_t blocks = (int64_t)n * (F / kQK8);
   const int grid = (int)((blocks + 7) / 8);
-  silu_mul_quantize_kernel<<<grid, 256, 0, stream>>>(gu, F, n, static_cast<uint8_t*>(xq), h_out);
-  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+  return launch_pdl(silu_mul_quantize_kernel, dim3(grid), dim3(256), 0, stream, gu, F, n,
+                    static_cast<uint8_t*>(xq), h_out);
 }
 
 }  // namespace mmvq

@@ -40,6 +40,9 @@ __device__ __forceinline__ ChunkMap chunk_map(int q) {
 __global__ void __launch_bounds__(256) repack_planar_kernel(const uint8_t* __restrict__ W,
                                                             int64_t rows, int nb,
                                                             uint8_t* __restrict__ P) {
+  // Writes weights: no early launch of the next kernel, whose weight
+  // stream may start before its own griddepcontrol.wait.
+  grid_dependency_wait();
   const int64_t t = blockIdx.x;
   const int64_t g = t / nb;
   const int b = (int)(t - g * nb);
@@ -76,6 +79,9 @@ __global__ void __launch_bounds__(256) gather_planar_kernel(const uint8_t* __res
                                                             const int32_t* __restrict__ row_ids,
                                                             int n, uint8_t* __restrict__ out,
                                                             int32_t* __restrict__ status) {
+  // Writes weights: no early launch of the next kernel, whose weight
+  // stream may start before its own griddepcontrol.wait.
+  grid_dependency_wait();
   const int64_t t = blockIdx.x;
   const int64_t g = t / nb;
   const int b = (int)(t - g * nb);
@@ -138,6 +144,7 @@ __global__ void __launch_bounds__(1024) route_groups_kernel(const int32_t* __res
   __shared__ int cnt[4096];
   __shared__ int wsum[33];
   const int tid = threadIdx.x;
+  grid_launch_dependents();
   grid_dependency_wait();
   for (int e = tid; e < n_experts; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -218,9 +225,8 @@ int launch_repack_planar(const void* W, int64_t rows, int K, void* P, cudaStream
   const int nb = K / kQK;
   const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * nb;
   if (tiles > 0x7fffffff) return MMVQ_ERR_SHAPE;
-  repack_planar_kernel<<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint8_t*>(W), rows, nb,
-                                                       static_cast<uint8_t*>(P));
-  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+  return launch_pdl(repack_planar_kernel, dim3((unsigned)tiles), dim3(256), 0, s,
+                    static_cast<const uint8_t*>(W), rows, nb, static_cast<uint8_t*>(P));
 }
 
 int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_ids, int n,
@@ -228,18 +234,16 @@ int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_
   const int nb = K / kQK;
   const int64_t tiles = ((int64_t)(n + kTileRows - 1) / kTileRows) * nb;
   if (tiles > 0x7fffffff) return MMVQ_ERR_SHAPE;
-  gather_planar_kernel<<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint8_t*>(P), rows, nb,
-                                                       row_ids, n, static_cast<uint8_t*>(out),
-                                                       status);
-  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+  return launch_pdl(gather_planar_kernel, dim3((unsigned)tiles), dim3(256), 0, s,
+                    static_cast<const uint8_t*>(P), rows, nb, row_ids, n,
+                    static_cast<uint8_t*>(out), status);
 }
 
 int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
                         int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
                         cudaStream_t s) {
-  route_groups_kernel<<<1, 1024, 0, s>>>(topk, T * k, k, n_experts, expert_ids, offsets, act_index,
-                                         slot_of, status);
-  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
+  return launch_pdl(route_groups_kernel, dim3(1), dim3(1024), 0, s, topk, T * k, k, n_experts,
+                    expert_ids, offsets, act_index, slot_of, status);
 }
 
 }  // namespace mmvq

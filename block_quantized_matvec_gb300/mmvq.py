@@ -40,6 +40,7 @@ SIGNATURES = {
     "mmvq_planar_bytes": (_I64, [_I64, _I]),
     "mmvq_repack_planar": (_I, [_I, _P, _I64, _I, _P, _P]),
     "mmvq_gather_planar_rows": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P]),
+    "mmvq_read_device_fault": (_I, [_P, _P]),
 }
 
 
@@ -180,6 +181,13 @@ def silu_mul_quantize_q8_1(gu: torch.Tensor, F: int, out: torch.Tensor | None = 
     _check(lib().mmvq_silu_mul_quantize_q8_1(_ptr(gu), F, n, _ptr(out), _ptr(h_out),
                                              _stream(stream)), "mmvq_silu_mul_quantize_q8_1")
     return out
+
+
+def read_device_fault(stream=None) -> int:
+    """Synchronise the stream, return and clear the device fault word (0 = none)."""
+    v = ctypes.c_int(0)
+    _check(lib().mmvq_read_device_fault(ctypes.byref(v), _stream(stream)), "mmvq_read_device_fault")
+    return v.value
 
 
 def planar_bytes(rows: int, K: int) -> int:

@@ -191,6 +191,17 @@ MMVQ_API int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int 
 MMVQ_API int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int32_t* row_ids,
                             int n, void* out, int32_t* status, mmvq_stream_t stream);
 
+/*
+ * Device fault word of the bulk-copy kernels.  Every wait of those kernels
+ * on a shared-memory barrier is bounded (about one second); a wait that
+ * runs out sets a bit here (1: barrier wait timed out) instead of hanging,
+ * and the kernel returns with its outputs undefined.  Synchronises
+ * `stream`, stores the word in *fault and clears it.  This HOST-pointer
+ * call blocks; it is not part of the hot path.  No counterpart on the
+ * pages (their kernels have no such waits).
+ */
+MMVQ_API int mmvq_read_device_fault(int* fault, mmvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
