@@ -9,7 +9,7 @@ namespace mmvq {
 int launch_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq, cudaStream_t s);
 int launch_silu_mul_quantize(const float* gu, int F, int n, void* xq, float* h_out, cudaStream_t s);
 int launch_dense(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
-                 int32_t* sumi, cudaStream_t s);
+                 int32_t* sumi, uint32_t flags, cudaStream_t s);
 int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,
                    const int32_t* expert_ids, const int32_t* offsets, int n_groups,
                    const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
@@ -18,6 +18,7 @@ int launch_repack_planar(const void* W, int64_t rows, int K, void* P, cudaStream
 int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_ids, int n,
                          void* out, int32_t* status, cudaStream_t s);
 int read_device_fault(int* fault, cudaStream_t stream);
+int dense_shape(int type, int64_t rows, int K, int ncols, int32_t* info);
 int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
                         int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
                         cudaStream_t s);
@@ -76,7 +77,15 @@ int mmvq_gemv(int type, const void* W, int64_t rows, int K, const void* xq, int 
               mmvq_stream_t stream) {
   const int rc = gemv_checks(type, W, rows, K, xq, ncols, y);
   if (rc) return rc;
-  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, nullptr, (cudaStream_t)stream);
+  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, nullptr, 0u, (cudaStream_t)stream);
+}
+
+int mmvq_gemv_ex(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
+                 unsigned int flags, mmvq_stream_t stream) {
+  const int rc = gemv_checks(type, W, rows, K, xq, ncols, y);
+  if (rc) return rc;
+  if (flags & ~(unsigned int)MMVQ_FLAG_XQ_STABLE) return MMVQ_ERR_SHAPE;
+  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, nullptr, flags, (cudaStream_t)stream);
 }
 
 int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
@@ -85,7 +94,7 @@ int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const vo
   if (rc) return rc;
   if (!y) return MMVQ_ERR_NULL;
   if (!aligned(y, 4)) return MMVQ_ERR_ALIGN;
-  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, sumi, (cudaStream_t)stream);
+  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, sumi, 0u, (cudaStream_t)stream);
 }
 
 int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, int K,
@@ -155,6 +164,15 @@ int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int
     return MMVQ_ERR_ALIGN;
   return mmvq::launch_gather_planar(W_planar, rows, K, row_ids, n, out, status,
                                     (cudaStream_t)stream);
+}
+
+int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
+  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K && type != MMVQ_Q6_K_PLANAR) return MMVQ_ERR_TYPE;
+  if (!info) return MMVQ_ERR_NULL;
+  const int rc = check_weights_shape(rows, K);
+  if (rc) return rc;
+  if (ncols < 1 || ncols > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
+  return mmvq::dense_shape(type, rows, K, ncols, info);
 }
 
 int mmvq_read_device_fault(int* fault, mmvq_stream_t stream) {

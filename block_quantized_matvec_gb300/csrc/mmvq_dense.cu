@@ -236,6 +236,35 @@ static int launch_dense_t(const uint8_t* W, int64_t rows, int K, const uint8_t* 
                     cfg.smem, stream, W, rows, K, xq, y, sumi);
 }
 
+template <int LAYOUT, int NCOLS>
+static int dense_shape_t(int64_t rows, int K, int32_t* info) {
+  DenseCfg cfg;
+  const int rc = dense_config<LAYOUT, NCOLS>(rows, K, &cfg);
+  if (rc != MMVQ_OK) return rc;
+  info[0] = cfg.grid;
+  info[1] = 32 * cfg.wk * cfg.wr;
+  info[2] = (int32_t)cfg.smem;
+  info[3] = cfg.wr;
+  info[4] = cfg.wk;
+  info[5] = 0;
+  return MMVQ_OK;
+}
+
+template <int LAYOUT>
+static int dense_shape_layout(int64_t rows, int K, int ncols, int32_t* info) {
+  switch (ncols) {
+    case 1: return dense_shape_t<LAYOUT, 1>(rows, K, info);
+    case 2: return dense_shape_t<LAYOUT, 2>(rows, K, info);
+    case 3: return dense_shape_t<LAYOUT, 3>(rows, K, info);
+    case 4: return dense_shape_t<LAYOUT, 4>(rows, K, info);
+    case 5: return dense_shape_t<LAYOUT, 5>(rows, K, info);
+    case 6: return dense_shape_t<LAYOUT, 6>(rows, K, info);
+    case 7: return dense_shape_t<LAYOUT, 7>(rows, K, info);
+    case 8: return dense_shape_t<LAYOUT, 8>(rows, K, info);
+  }
+  return MMVQ_ERR_NCOLS;
+}
+
 template <int LAYOUT>
 static int launch_dense_layout(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, int ncols,
                                float* y, int32_t* sumi, cudaStream_t s) {
@@ -252,15 +281,26 @@ static int launch_dense_layout(const uint8_t* W, int64_t rows, int K, const uint
   return MMVQ_ERR_NCOLS;
 }
 
+int q6_planar_tma_shape(int64_t rows, int K, int ncols, int32_t* info);
+
+int dense_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
+  switch (type) {
+    case MMVQ_Q6_K_PLANAR: return q6_planar_tma_shape(rows, K, ncols, info);
+    case MMVQ_Q6_K: return dense_shape_layout<kQ6Gguf>(rows, K, ncols, info);
+    case MMVQ_Q4_K: return dense_shape_layout<kQ4Gguf>(rows, K, ncols, info);
+  }
+  return MMVQ_ERR_TYPE;
+}
+
 int launch_q6_planar_tma(const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
-                         int32_t* sumi, cudaStream_t s);
+                         int32_t* sumi, uint32_t flags, cudaStream_t s);
 
 int launch_dense(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
-                 int32_t* sumi, cudaStream_t s) {
+                 int32_t* sumi, uint32_t flags, cudaStream_t s) {
   const uint8_t* w = static_cast<const uint8_t*>(W);
   const uint8_t* x = static_cast<const uint8_t*>(xq);
   switch (type) {
-    case MMVQ_Q6_K_PLANAR: return launch_q6_planar_tma(W, rows, K, xq, ncols, y, sumi, s);
+    case MMVQ_Q6_K_PLANAR: return launch_q6_planar_tma(W, rows, K, xq, ncols, y, sumi, flags, s);
     case MMVQ_Q6_K: return launch_dense_layout<kQ6Gguf>(w, rows, K, x, ncols, y, sumi, s);
     case MMVQ_Q4_K: return launch_dense_layout<kQ4Gguf>(w, rows, K, x, ncols, y, sumi, s);
   }

@@ -88,9 +88,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
 
 // Tile bytes of lane L out of a ring slot: the same offsets as in global
 // memory, so each warp-wide 16-byte load covers 512 consecutive bytes.
@@ -118,31 +115,42 @@ __device__ __forceinline__ void load_q6_tile_smem(const uint8_t* tile, int lane,
 }
 
 // Shared memory: [full S][empty S] mbarriers, a fail flag, the ring
-// (S stages of C tiles, 128-byte aligned), the activation quants and d, the
-// K-slice partials [C][8][16].
+// (S stages of G*P tiles, 128-byte aligned), the activation quants, d_a as
+// floats, the K-slice partials [C][8][16].
 __host__ __device__ inline size_t tma_ring_offset(int S) { return ((size_t)16 * S + 16 + 127) & ~size_t(127); }
-__host__ __device__ inline size_t tma_smem_bytes(int S, int K, int ncols, int C) {
+__host__ __device__ inline size_t tma_smem_bytes(int S, int K, int ncols, int G, int P) {
+  const int C = G * P;
   return tma_ring_offset(S) + (size_t)S * C * kTileBytes + (size_t)ncols * act_row_bytes(K) +
          (size_t)ncols * (K / kQK8) * 4 + (size_t)C * kMaxCols * kTileRows * 4;
 }
 
+__device__ __forceinline__ void group_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Consumers are G groups of P warps (C = G*P); warp C is the producer.  A
+// batch is G of the CTA's row groups (group g takes the g-th); within a
+// batch, stage bb holds, for each group, the P consecutive tiles
+// bb*P .. bb*P+P-1 of its row group, and warp (g, p) takes tile bb*P+p.  The
+// P partial sums of a row group are added in warp order at the batch end.
 template <int NCOLS>
 __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __restrict__ W,
                                                                int64_t rows, int K,
                                                                const uint8_t* __restrict__ xq,
                                                                float* __restrict__ y,
-                                                               int32_t* __restrict__ sumi, int S) {
+                                                               int32_t* __restrict__ sumi, int S,
+                                                               int G, int P, uint32_t flags) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int C = (int)(blockDim.x >> 5) - 1;  // consumer warps; warp C produces
+  const int C = G * P;  // consumer warps; warp C produces
   const int nb = K / kQK;
   const int nbq = K / kQK8;
   const int rb = act_row_bytes(K);
   const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
-
-  const int spr = nb / C;  // stages per row group
+  const int spb = nb / P;  // stages per batch
   const size_t stage_bytes = (size_t)C * kTileBytes;
+
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + S;
   volatile int* fail = reinterpret_cast<volatile int*>(empty + S);
@@ -164,7 +172,8 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
 
   // this CTA's row groups: blockIdx.x, + gridDim.x, ...
   const int64_t my_rgs = (blockIdx.x < n_rg) ? (n_rg - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int64_t total = my_rgs * spr;
+  const int64_t batches = (my_rgs + G - 1) / G;
+  const int64_t total = batches * spb;
 
   if (warp == C) {  // ------------------------------------------ producer
     if (lane == 0) {
@@ -177,11 +186,17 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
           atomicOr(&g_fault_word, kFaultMbarTimeout);
         }
         if (*fail) break;
-        const int64_t rg = blockIdx.x + (it / spr) * gridDim.x;
-        const int b0 = (int)(it % spr) * C;
-        mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
-        bulk_g2s(ring + (size_t)s * stage_bytes, W + (rg * nb + b0) * kTileBytes,
-                 (uint32_t)stage_bytes, &full[s]);
+        const int64_t j = it / spb;
+        const int bb = (int)(it % spb);
+        const int64_t left = my_rgs - j * G;
+        const int valid = (int)(left < G ? left : G);
+        mbar_expect_tx(&full[s], (uint32_t)(valid * P * kTileBytes));
+        for (int g = 0; g < valid; ++g) {
+          const int64_t rg = blockIdx.x + (j * G + g) * (int64_t)gridDim.x;
+          bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)g * P * kTileBytes,
+                   W + (rg * nb + (int64_t)bb * P) * kTileBytes, (uint32_t)(P * kTileBytes),
+                   &full[s]);
+        }
       }
       // no copy of this CTA may land after it exits: wait (bounded) for the
       // last phase of every slot that was filled
@@ -197,37 +212,54 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
   // ------------------------------------------------------------ consumers
   const int nthreads = 32 * C;
   const int tid = threadIdx.x;
-  grid_dependency_wait();
+  // With MMVQ_FLAG_XQ_STABLE no kernel that may still run writes xq, so the
+  // whole product runs before the grid dependency; only the stores of y
+  // wait for the preceding kernel.
+  const bool stable = (flags & MMVQ_FLAG_XQ_STABLE) != 0;
+  bool waited = !stable;
+  if (!stable) grid_dependency_wait();
   stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da, nullptr, tid, nthreads);
-  consumer_sync(nthreads);
+  group_sync(1, nthreads);
 
+  const int g = warp / P;
+  const int p = warp - g * P;
   const int i = lane & 15;
   const int h = lane >> 4;
-  for (int64_t k = 0; k < my_rgs; ++k) {
-    const int64_t rg = blockIdx.x + k * gridDim.x;
+  for (int64_t j = 0; j < batches; ++j) {
+    const int64_t k = j * G + g;
+    const bool valid = k < my_rgs;
+    const int64_t rg = blockIdx.x + k * (int64_t)gridDim.x;
     const int64_t row = rg * kTileRows + i;
-    int32_t* srow = (sumi && row < rows) ? sumi + row * nbq : nullptr;
+    int32_t* srow = (sumi && valid && row < rows) ? sumi + row * nbq : nullptr;
+    if (srow && !waited) {
+      grid_dependency_wait();
+      waited = true;
+    }
     float acc[NCOLS];
 #pragma unroll
     for (int c = 0; c < NCOLS; ++c) acc[c] = 0.0f;
-    for (int j = 0; j < spr; ++j) {
-      const int64_t it = k * spr + j;
+    for (int bb = 0; bb < spb; ++bb) {
+      const int64_t it = j * spb + bb;
       const int s = (int)(it % S);
       if (!*fail && !mbar_wait(&full[s], (uint32_t)((it / S) & 1))) {
         *fail = 1;
         atomicOr(&g_fault_word, kFaultMbarTimeout);
       }
       Q6Half w;
-      load_q6_tile_smem(ring + (size_t)s * stage_bytes + (size_t)warp * kTileBytes, lane, w);
+      if (valid) load_q6_tile_smem(ring + (size_t)s * stage_bytes + (size_t)warp * kTileBytes, lane, w);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      q6_dot<NCOLS>(w, h, j * C + warp, act, rb, da, nbq, acc, srow, rows * nbq);
+      if (valid) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, rows * nbq);
     }
-    // halves of each row, then the K-slices in warp order
+    // halves of each row, then the group's K-slices in warp order
 #pragma unroll
     for (int c = 0; c < NCOLS; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
-    if (C == 1) {
-      if (h == 0 && row < rows) {
+    if (!waited) {
+      grid_dependency_wait();
+      waited = true;
+    }
+    if (P == 1) {
+      if (valid && h == 0 && row < rows) {
 #pragma unroll
         for (int c = 0; c < NCOLS; ++c) y[c * rows + row] = acc[c];
       }
@@ -237,30 +269,32 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
 #pragma unroll
       for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
     }
-    consumer_sync(nthreads);
-    if (warp == 0 && h == 0 && row < rows) {
+    group_sync(2 + g, 32 * P);
+    if (p == 0 && valid && h == 0 && row < rows) {
 #pragma unroll
       for (int c = 0; c < NCOLS; ++c) {
         float sum = 0.0f;
-        for (int wq = 0; wq < C; ++wq) sum += red[(wq * kMaxCols + c) * kTileRows + i];
+        for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
         y[c * rows + row] = sum;
       }
     }
-    consumer_sync(nthreads);
+    group_sync(2 + g, 32 * P);
   }
 }
 
 // ------------------------------------------------------------ host side ----
 
 struct TmaCfg {
-  int consumers, slots, grid;
+  int G, P, slots, grid;
   size_t smem;
 };
 
-// Consumers C: a divisor of K/256 (each row group's blocks split evenly),
-// as many as possible up to 12 while the ring still holds two stages.  Ring
-// depth: as many stages as fit in about 110 KB of shared memory (so this
-// call's CTA and the next call's can share an SM), and at least two.
+// Launch shape.  Candidates (G, P) with P | K/256 and C = G*P <= 12; the ring
+// gets as many stages as fit in ~110 KB (two CTAs per SM when registers
+// allow), at least two.  Cost model: a CTA's time is its batches x stages
+// per batch, each stage one tile per consumer warp; the SM's issue rate is
+// shared by all resident consumer warps.  The cheapest shape wins; ties go
+// to more consumer warps.
 template <int NCOLS>
 static int tma_config(int64_t rows, int K, TmaCfg* out) {
   static std::mutex mu;
@@ -280,59 +314,104 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
   const size_t limit = max_smem_optin();
   if (sms <= 0 || limit == 0) return MMVQ_ERR_CUDA;
   const int nb = K / kQK;
+  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
   const size_t budget = std::min<size_t>(limit, 110 * 1024);
-  int C = 0, S = 0;
-  size_t smem = 0;
-  for (int d = std::min(nb, 12); d >= 1 && C == 0; --d) {
-    if (nb % d) continue;
-    for (int s = 64; s >= 2; --s) {
-      const size_t b = tma_smem_bytes(s, K, NCOLS, d);
-      if (b <= budget || (s == 2 && b <= limit)) {
-        C = d;
-        S = s;
-        smem = b;
-        break;
+  TmaCfg best = {0, 0, 0, 0, 0};
+  double best_cost = 1e300;
+  int best_c = 0;
+  for (int P = 1; P <= std::min(nb, 12); ++P) {
+    if (nb % P) continue;
+    for (int G = 1; G * P <= 12; ++G) {
+      int S = 0;
+      size_t smem = 0;
+      for (int s = 32; s >= 2; --s) {
+        const size_t b = tma_smem_bytes(s, K, NCOLS, G, P);
+        if (b <= budget || (s == 2 && b <= limit)) {
+          S = s;
+          smem = b;
+          break;
+        }
+      }
+      if (S == 0) continue;
+      if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (G * P + 1), smem) !=
+          cudaSuccess)
+        return MMVQ_ERR_CUDA;
+      if (per_sm < 1) continue;
+      const int64_t ctas = std::min<int64_t>((n_rg + G - 1) / G, (int64_t)sms * per_sm);
+      const int64_t rgs_per_cta = (n_rg + ctas - 1) / ctas;
+      const int64_t batches = (rgs_per_cta + G - 1) / G;
+      const double ctas_per_sm = std::min<double>(per_sm, (double)ctas / sms);
+      const double warps_per_sm = std::max(1.0, ctas_per_sm) * G * P;
+      // stage time: one tile per warp, slowed once the SM holds > 16 warps
+      const double stage = std::max(1.0, warps_per_sm / 16.0);
+      const double cost = (double)batches * (nb / P) * stage;
+      if (cost < best_cost * 0.999 || (cost < best_cost * 1.001 && G * P > best_c)) {
+        best_cost = cost;
+        best_c = G * P;
+        best = {G, P, S, (int)ctas, smem};
       }
     }
   }
-  if (C == 0) return MMVQ_ERR_SHAPE;
-  if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (C + 1), smem) !=
-          cudaSuccess ||
-      per_sm < 1)
-    return MMVQ_ERR_CUDA;
-  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
-  TmaCfg cfg = {C, S, (int)std::min<int64_t>(n_rg, (int64_t)sms * per_sm), smem};
+  if (best.G == 0) return MMVQ_ERR_SHAPE;
   std::lock_guard<std::mutex> lock(mu);
-  cache[key] = cfg;
-  *out = cfg;
+  cache[key] = best;
+  *out = best;
   return MMVQ_OK;
 }
 
 template <int NCOLS>
 static int launch_tma_t(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
-                        int32_t* sumi, cudaStream_t stream) {
+                        int32_t* sumi, uint32_t flags, cudaStream_t stream) {
   TmaCfg cfg;
   const int rc = tma_config<NCOLS>(rows, K, &cfg);
   if (rc != MMVQ_OK) return rc;
-  return launch_pdl(mmvq_q6p_tma_kernel<NCOLS>, dim3(cfg.grid), dim3(32 * (cfg.consumers + 1)),
-                    cfg.smem, stream, W, rows, K, xq, y, sumi, cfg.slots);
+  return launch_pdl(mmvq_q6p_tma_kernel<NCOLS>, dim3(cfg.grid), dim3(32 * (cfg.G * cfg.P + 1)),
+                    cfg.smem, stream, W, rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, flags);
 }
 
 int launch_q6_planar_tma(const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
-                         int32_t* sumi, cudaStream_t s) {
+                         int32_t* sumi, uint32_t flags, cudaStream_t s) {
   const uint8_t* w = static_cast<const uint8_t*>(W);
   const uint8_t* x = static_cast<const uint8_t*>(xq);
   switch (ncols) {
-    case 1: return launch_tma_t<1>(w, rows, K, x, y, sumi, s);
-    case 2: return launch_tma_t<2>(w, rows, K, x, y, sumi, s);
-    case 3: return launch_tma_t<3>(w, rows, K, x, y, sumi, s);
-    case 4: return launch_tma_t<4>(w, rows, K, x, y, sumi, s);
-    case 5: return launch_tma_t<5>(w, rows, K, x, y, sumi, s);
-    case 6: return launch_tma_t<6>(w, rows, K, x, y, sumi, s);
-    case 7: return launch_tma_t<7>(w, rows, K, x, y, sumi, s);
-    case 8: return launch_tma_t<8>(w, rows, K, x, y, sumi, s);
+    case 1: return launch_tma_t<1>(w, rows, K, x, y, sumi, flags, s);
+    case 2: return launch_tma_t<2>(w, rows, K, x, y, sumi, flags, s);
+    case 3: return launch_tma_t<3>(w, rows, K, x, y, sumi, flags, s);
+    case 4: return launch_tma_t<4>(w, rows, K, x, y, sumi, flags, s);
+    case 5: return launch_tma_t<5>(w, rows, K, x, y, sumi, flags, s);
+    case 6: return launch_tma_t<6>(w, rows, K, x, y, sumi, flags, s);
+    case 7: return launch_tma_t<7>(w, rows, K, x, y, sumi, flags, s);
+    case 8: return launch_tma_t<8>(w, rows, K, x, y, sumi, flags, s);
+  }
+  return MMVQ_ERR_NCOLS;
+}
+
+template <int NCOLS>
+static int tma_shape_t(int64_t rows, int K, int32_t* info) {
+  TmaCfg cfg;
+  const int rc = tma_config<NCOLS>(rows, K, &cfg);
+  if (rc != MMVQ_OK) return rc;
+  info[0] = cfg.grid;
+  info[1] = 32 * (cfg.G * cfg.P + 1);
+  info[2] = (int32_t)cfg.smem;
+  info[3] = cfg.G;
+  info[4] = cfg.P;
+  info[5] = cfg.slots;
+  return MMVQ_OK;
+}
+
+int q6_planar_tma_shape(int64_t rows, int K, int ncols, int32_t* info) {
+  switch (ncols) {
+    case 1: return tma_shape_t<1>(rows, K, info);
+    case 2: return tma_shape_t<2>(rows, K, info);
+    case 3: return tma_shape_t<3>(rows, K, info);
+    case 4: return tma_shape_t<4>(rows, K, info);
+    case 5: return tma_shape_t<5>(rows, K, info);
+    case 6: return tma_shape_t<6>(rows, K, info);
+    case 7: return tma_shape_t<7>(rows, K, info);
+    case 8: return tma_shape_t<8>(rows, K, info);
   }
   return MMVQ_ERR_NCOLS;
 }

@@ -46,7 +46,8 @@ __device__ __forceinline__ void quantize_lane(float v, uint8_t* out, int lane) {
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int K,
                                                             int ncols, int64_t ldx,
                                                             uint8_t* __restrict__ xq) {
-  grid_launch_dependents();
+  // Writes activations: the next kernel may not start before this one ends
+  // (no early trigger), which is what MMVQ_FLAG_XQ_STABLE relies on.
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int nbq = K / kQK8;
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
 __global__ void __launch_bounds__(256) silu_mul_quantize_kernel(const float* __restrict__ gu, int F,
                                                                 int n, uint8_t* __restrict__ xq,
                                                                 float* __restrict__ h_out) {
-  grid_launch_dependents();
+  // Writes activations: no early start of the next kernel (see above).
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int nbq = F / kQK8;

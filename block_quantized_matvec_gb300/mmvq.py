@@ -24,6 +24,7 @@ Q8_1_BYTES = 36
 MAX_COLS = 8
 
 OK = 0
+FLAG_XQ_STABLE = 1
 ERR_TYPE, ERR_SHAPE, ERR_NCOLS, ERR_NULL, ERR_ALIGN, ERR_ROUTING, ERR_CUDA = -1, -2, -3, -4, -5, -6, -7
 
 # name -> (restype, argtypes); mirrors include/mmvq.h
@@ -33,6 +34,7 @@ SIGNATURES = {
     "mmvq_strerror": (ctypes.c_char_p, [_I]),
     "mmvq_quantize_q8_1": (_I, [_P, _I, _I, _I64, _P, _P]),
     "mmvq_gemv": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P]),
+    "mmvq_gemv_ex": (_I, [_I, _P, _I64, _I, _P, _I, _P, ctypes.c_uint, _P]),
     "mmvq_debug_block_sums": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P, _P]),
     "mmvq_grouped": (_I, [_I, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P]),
     "mmvq_route_groups": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
@@ -41,6 +43,7 @@ SIGNATURES = {
     "mmvq_repack_planar": (_I, [_I, _P, _I64, _I, _P, _P]),
     "mmvq_gather_planar_rows": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P]),
     "mmvq_read_device_fault": (_I, [_P, _P]),
+    "mmvq_launch_shape": (_I, [_I, _I64, _I, _I, _P]),
 }
 
 
@@ -116,14 +119,19 @@ def quantize_q8_1(x: torch.Tensor, K: int | None = None, out: torch.Tensor | Non
 
 
 def gemv(type_: int, W: torch.Tensor, rows: int, K: int, xq: torch.Tensor, ncols: int,
-         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y [ncols, rows] fp32 = W (rows x K, block type ``type_``) times ncols Q8_1 columns."""
+         out: torch.Tensor | None = None, stream=None, flags: int = 0) -> torch.Tensor:
+    """y [ncols, rows] fp32 = W (rows x K, block type ``type_``) times ncols Q8_1 columns.
+    flags: FLAG_XQ_STABLE when no still-running kernel writes xq (mmvq_gemv_ex)."""
     _dev(W, "W")
     _dev(xq, "xq")
     if out is None:
         out = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
-    _check(lib().mmvq_gemv(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(out), _stream(stream)),
-           "mmvq_gemv")
+    if flags:
+        _check(lib().mmvq_gemv_ex(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(out), flags,
+                                  _stream(stream)), "mmvq_gemv_ex")
+    else:
+        _check(lib().mmvq_gemv(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(out),
+                               _stream(stream)), "mmvq_gemv")
     return out
 
 
@@ -181,6 +189,15 @@ def silu_mul_quantize_q8_1(gu: torch.Tensor, F: int, out: torch.Tensor | None = 
     _check(lib().mmvq_silu_mul_quantize_q8_1(_ptr(gu), F, n, _ptr(out), _ptr(h_out),
                                              _stream(stream)), "mmvq_silu_mul_quantize_q8_1")
     return out
+
+
+def launch_shape(type_: int, rows: int, K: int, ncols: int) -> dict:
+    """The launch shape mmvq_gemv picks (host-only query)."""
+    info = (ctypes.c_int32 * 6)()
+    _check(lib().mmvq_launch_shape(type_, rows, K, ncols, info), "mmvq_launch_shape")
+    keys = (["grid", "threads", "smem", "G", "P", "stages"] if type_ == TYPE_Q6_K_PLANAR
+            else ["grid", "threads", "smem", "WR", "WK", "unused"])
+    return dict(zip(keys, list(info)))
 
 
 def read_device_fault(stream=None) -> int:

@@ -77,6 +77,17 @@ enum mmvq_type {
   MMVQ_Q6_K_PLANAR = 1014 /* Q6_K in 16-row planar tiles (see above) */
 };
 
+/* Flags of mmvq_gemv_ex. */
+enum mmvq_flags {
+  /* xq is stable: no kernel that may still be running when this call starts
+   * writes it (true when xq came from mmvq_quantize_q8_1 or
+   * mmvq_silu_mul_quantize_q8_1, or earlier work, and nothing launched
+   * since writes it; those quantisers never let their successor start
+   * early).  The product then runs before waiting for the preceding kernel,
+   * and only the stores of y wait for it. */
+  MMVQ_FLAG_XQ_STABLE = 1
+};
+
 enum mmvq_status {
   MMVQ_OK = 0,
   MMVQ_ERR_TYPE = -1,    /* type not supported by this entry point */
@@ -115,6 +126,19 @@ MMVQ_API int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, v
  */
 MMVQ_API int mmvq_gemv(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
               mmvq_stream_t stream);
+
+/*
+ * mmvq_gemv with launch flags (mmvq_flags; 0 gives mmvq_gemv).  With
+ * MMVQ_FLAG_XQ_STABLE, consecutive calls that share one quantised
+ * activation (several matrices reading one input, like q/k/v or gate/up)
+ * overlap on the GPU: each call streams its weights and computes while the
+ * previous call is still finishing.  Weights are always streamed before the
+ * wait; no kernel of this library that writes weights (repack, gather)
+ * lets its successor start early.  Unknown flag bits: MMVQ_ERR_SHAPE.  The
+ * flag currently changes the schedule of MMVQ_Q6_K_PLANAR only.
+ */
+MMVQ_API int mmvq_gemv_ex(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
+                          float* y, unsigned int flags, mmvq_stream_t stream);
 
 /*
  * The per-32-block integer sums the dense product forms, for parity checks:
@@ -190,6 +214,16 @@ MMVQ_API int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int 
  */
 MMVQ_API int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int32_t* row_ids,
                             int n, void* out, int32_t* status, mmvq_stream_t stream);
+
+/*
+ * The launch shape mmvq_gemv picks for this matrix and column count, on the
+ * current device (host-only; no kernel runs).  info[6] (HOST memory):
+ * grid, threads per CTA, dynamic shared bytes, then for MMVQ_Q6_K_PLANAR
+ * G (row groups per batch), P (warps per row group), ring stages; for the
+ * GGUF types WR (row groups per CTA), WK (warps per row group), 0.
+ * Same argument rules as mmvq_gemv.  No counterpart on the pages.
+ */
+MMVQ_API int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info);
 
 /*
  * Device fault word of the bulk-copy kernels.  Every wait of those kernels
