@@ -46,6 +46,8 @@ UNIT = "GB/s"
 SWEEP_SHAPES = [(2560, 2560), (2560, 10240), (10240, 2560)]
 SWEEP_COLS = [1, 2, 4, 6, 8]
 HEAD_SHAPE = (151936, 2560)
+DRAFT_ROWS = 4096
+MOE = {"experts": 256, "hidden": 2560, "ffn": 768, "top_k": 8}
 Q4K_SHAPES = [(12288, 2560), (6144, 2560), (2560, 6144), (640, 2560), (512, 2560)]
 
 
@@ -56,8 +58,11 @@ def workload_cases(name):
     if name == "q6k_sweep_gguf":
         return [("q6_k", r, k, SWEEP_COLS) for r, k in SWEEP_SHAPES]
     if name == "lm_head":
-        return [("q6_k_planar", HEAD_SHAPE[0], HEAD_SHAPE[1], [1, 2, 3, 4, 5])]
+        return [("q6_k_planar", HEAD_SHAPE[0], HEAD_SHAPE[1], [1, 2, 3, 4, 5]),
+                ("q6_k_planar_draft", DRAFT_ROWS, HEAD_SHAPE[1], [1, 2, 3, 4, 5])]
     if name == "q4k_dense":
+        return [("q4_k_planar", r, k, [1, 4]) for r, k in Q4K_SHAPES]
+    if name == "q4k_dense_gguf":
         return [("q4_k", r, k, [1, 4]) for r, k in Q4K_SHAPES]
     raise SystemExit(f"unknown workload {name}")
 
@@ -65,8 +70,12 @@ def workload_cases(name):
 WORKLOAD_DESC = {
     "q6k_sweep": "Q6_K MMVQ sweep 2560x2560, 2560x10240, 10240x2560 (rows x K) at 1,2,4,6,8 cols, planar tiles",
     "q6k_sweep_gguf": "Q6_K MMVQ sweep 2560x2560, 2560x10240, 10240x2560 at 1,2,4,6,8 cols, GGUF blocks",
-    "lm_head": "Q6_K LM head 151936x2560 at 1-5 cols, planar tiles",
-    "q4k_dense": "Q4_K dense 12288x2560, 6144x2560, 2560x6144, 640x2560, 512x2560 at 1 and 4 cols",
+    "lm_head": "Q6_K LM head 151936x2560 at 1-5 cols, planar tiles; 4096-row draft head gathered from it",
+    "q4k_dense": "Q4_K dense 12288x2560, 6144x2560, 2560x6144, 640x2560, 512x2560 at 1 and 4 cols, planar tiles",
+    "q4k_dense_gguf": "Q4_K dense 12288x2560, 6144x2560, 2560x6144, 640x2560, 512x2560 at 1 and 4 cols, GGUF blocks",
+    "moe_t1": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=1 top-8 (planar experts)",
+    "moe_t4": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=4 top-8 (planar experts)",
+    "moe_t8": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=8 top-8 (planar experts)",
 }
 
 
@@ -179,18 +188,28 @@ def run_ours(args, rank, world, local_rank):
     mmvq.lib()
 
     cases_spec = workload_cases(args.workload)
-    type_of = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K}
+    type_of = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K,
+               "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR, "q6_k_planar_draft": mmvq.TYPE_Q6_K_PLANAR}
 
     # resident weights: copies per shape so that each shape's copies exceed 2x L2
     mats = []
     host_weights = []
     for si, (fmt, rows, K, cols) in enumerate(cases_spec):
-        gen = synth.q4_k_weights if fmt == "q4_k" else synth.q6_k_weights
-        W = gen(rows, K, salt=si)
-        host_weights.append(W)
-        Wd = torch.from_numpy(W.reshape(-1)).to(dev)
-        if fmt == "q6_k_planar":
-            Wd = mmvq.repack_planar(Wd, rows, K)
+        if fmt == "q6_k_planar_draft":
+            # the draft head: seeded rows gathered from the planar LM head above
+            head_rows = cases_spec[0][1]
+            ids = synth.draft_rows(rows, head_rows)
+            Wd, _ = mmvq.gather_planar_rows(mats[0][0], head_rows, K,
+                                            torch.from_numpy(ids).to(dev))
+            host_weights.append(np.ascontiguousarray(host_weights[0][ids]))
+        else:
+            gen = synth.q4_k_weights if fmt.startswith("q4_k") else synth.q6_k_weights
+            W = gen(rows, K, salt=si)
+            host_weights.append(W)
+            Wd = torch.from_numpy(W.reshape(-1)).to(dev)
+            if fmt in ("q6_k_planar", "q4_k_planar"):
+                Wd = mmvq.repack_planar(Wd, rows, K, type_=mmvq.TYPE_Q4_K if fmt == "q4_k_planar"
+                                        else mmvq.TYPE_Q6_K)
         nbytes = metrics.weight_bytes(fmt, rows, K)
         copies = max(2, math.ceil(2 * l2 / nbytes))
         mats.append([Wd] + [Wd.clone() for _ in range(copies - 1)])
@@ -355,13 +374,155 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
+
+# ------------------------------------------------------------- MoE step --
+
+def run_moe(args, rank, world, local_rank):
+    """One step = the routed-expert hot path for T tokens: Q8_1 quantise the
+    hidden states, per-expert token lists from the top-k routing, grouped
+    gate|up MMVQ, SiLU(gate)*up requantised to Q8_1, grouped down MMVQ.
+    Experts are planar Q4_K tiles; each step uses the next of 16 seeded
+    routings, so consecutive steps read different experts.  Weight bytes =
+    distinct experts read x (gate|up + down) bytes."""
+    import torch
+    from block_quantized_matvec_gb300 import metrics, mmvq, synth
+
+    T = int(args.workload.split("_t")[1])
+    E, H, F, k = MOE["experts"], MOE["hidden"], MOE["ffn"], MOE["top_k"]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    mmvq.lib()
+    q4 = mmvq.TYPE_Q4_K
+
+    def planar_experts(rows, K, salt):
+        host = synth.expert_weights("q4_k", E, rows, K, salt=salt)
+        per = mmvq.planar_bytes(rows, K, q4)
+        out = torch.empty(E * per, dtype=torch.uint8, device=dev)
+        for e in range(E):
+            mmvq.repack_planar(torch.from_numpy(host[e].reshape(-1)).to(dev), rows, K,
+                               out=out[e * per:(e + 1) * per], type_=q4)
+        return host, out
+
+    gu_host, W_gu = planar_experts(2 * F, H, 1)
+    dn_host, W_dn = planar_experts(H, F, 2)
+    R = 16
+    topks = [synth.routing(T, k, E, salt=100 + r) for r in range(R)]
+    topk_dev = [torch.from_numpy(t).to(dev) for t in topks]
+    x_host = synth.activations(H, T)
+    x_dev = torch.from_numpy(x_host).to(dev)
+    x_pinned = torch.from_numpy(x_host).pin_memory()
+    n = T * k
+    xq = torch.empty((T, H // 32, 36), dtype=torch.uint8, device=dev)
+    gu = torch.empty((n, 2 * F), device=dev)
+    hq = torch.empty((n, F // 32, 36), dtype=torch.uint8, device=dev)
+    y = torch.empty((n, H), device=dev)
+    y_pinned = torch.empty((n, H)).pin_memory()
+    torch.cuda.synchronize()
+
+    def step(r, s=None, evs=None):
+        rec = (lambda i: _record_external(evs[i], s)) if evs is not None else (lambda i: None)
+        rec(0)
+        mmvq.quantize_q8_1(x_dev, out=xq)
+        rec(1)
+        eids, offs, act, _, status = mmvq.route_groups(topk_dev[r], E)
+        rec(2)
+        mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_gu, E, 2 * F, H, eids, offs, act, xq, T, n, out=gu,
+                     status=status)
+        rec(3)
+        mmvq.silu_mul_quantize_q8_1(gu, F, out=hq)
+        rec(4)
+        mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_dn, E, H, F, eids, offs, None, hq, n, n, out=y,
+                     status=status)
+        rec(5)
+
+    for r in range(R):
+        step(r)
+    torch.cuda.synchronize()
+    graphs, events = [], []
+    for r in range(R):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for e in evs:
+            e.record()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+            step(r, torch.cuda.current_stream(), evs)
+        torch.cuda.synchronize()
+        graphs.append(g)
+        events.append(evs)
+
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    for i in range(args.warmup):
+        graphs[i % R].replay()
+    torch.cuda.synchronize()
+    clocks.wait_first_sample()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark()
+    t0.record(stream)
+    for i in range(args.steps):
+        graphs[i % R].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+
+    distinct = [len(np.unique(t)) for t in topks]
+    step_bytes = [metrics.moe_step_bytes(d, H, F) for d in distinct]
+    total_bytes = sum(step_bytes[i % R] for i in range(args.steps))
+    names = ["quantize", "route", "grouped_gate_up", "silu_requant", "grouped_down"]
+    dur = np.array([[evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(5)] for evs in events])
+    mean_us = dur.mean(axis=0)
+    gu_bytes = np.mean([d * metrics.weight_bytes("q4_k", 2 * F, H) for d in distinct])
+    dn_bytes = np.mean([d * metrics.weight_bytes("q4_k", H, F) for d in distinct])
+    peak, peak_kind = load_peak()
+    achieved = gu_bytes / (mean_us[2] * 1e-6) / 1e9
+
+    e2e_steps = max(3, min(args.steps, 200))
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for i in range(e2e_steps):
+        x_dev.copy_(x_pinned, non_blocking=True)
+        graphs[i % R].replay()
+        y_pinned.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - w0) / e2e_steps
+
+    out = {
+        "metric": METRIC, "value": round(total_bytes / (elapsed_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a + fp32",
+        "data": "synthetic (seeded generators shaped like the pages' matrices)",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "tokens": T, "routings": R,
+                   "distinct_experts_mean": float(np.mean(distinct)),
+                   "timing": "CUDA graph replay; event nodes between the five kernels"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "grouped gate|up MMVQ"},
+        "e2e": {"value": round(np.mean(step_bytes) / e2e_s / 1e9, 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y.numel() * 4),
+                "steps": e2e_steps},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+        "kernels_us": {nm: round(float(v), 3) for nm, v in zip(names, mean_us)},
+        "grouped_gbps": {"gate_up": round(gu_bytes / mean_us[2] / 1e3, 1),
+                         "down": round(dn_bytes / mean_us[4] / 1e3, 1)},
+    }
+    return out
+
 # ---------------------------------------------------------- CPU oracle --
 
 def _oracle_pass(cases_spec, host_weights, row_sample, salt0=0):
     """One pass of the oracle over every case; returns (weight bytes, seconds)."""
     import oracle
     from block_quantized_matvec_gb300 import metrics, synth
-    tcode = {"q6_k_planar": oracle.TYPE_Q6_K, "q6_k": oracle.TYPE_Q6_K, "q4_k": oracle.TYPE_Q4_K}
+    tcode = {"q6_k_planar": oracle.TYPE_Q6_K, "q6_k": oracle.TYPE_Q6_K, "q4_k": oracle.TYPE_Q4_K,
+             "q4_k_planar": oracle.TYPE_Q4_K, "q6_k_planar_draft": oracle.TYPE_Q6_K}
     nbytes = 0
     secs = 0.0
     for si, (fmt, rows, K, cols) in enumerate(cases_spec):
@@ -404,7 +565,7 @@ def run_reference(args, rank, world):
     sample_rows = 64
     host_weights = []
     for si, (fmt, rows, K, cols) in enumerate(cases_spec):
-        gen = synth.q4_k_weights if fmt == "q4_k" else synth.q6_k_weights
+        gen = synth.q4_k_weights if fmt.startswith("q4_k") else synth.q6_k_weights
         host_weights.append(np.ascontiguousarray(gen(min(rows, sample_rows), K, salt=si)))
     for _ in range(args.warmup):
         _oracle_pass(cases_spec, host_weights, sample_rows)
@@ -484,7 +645,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    res = run_ours(args, rank, world, local_rank)
+    if args.workload.startswith("moe_"):
+        res = run_moe(args, rank, world, local_rank)
+    else:
+        res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

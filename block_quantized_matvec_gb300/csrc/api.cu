@@ -14,7 +14,7 @@ int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,
                    const int32_t* expert_ids, const int32_t* offsets, int n_groups,
                    const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
                    int32_t* status, cudaStream_t s);
-int launch_repack_planar(const void* W, int64_t rows, int K, void* P, cudaStream_t s);
+int launch_repack_planar(int type, const void* W, int64_t rows, int K, void* P, cudaStream_t s);
 int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_ids, int n,
                          void* out, int32_t* status, cudaStream_t s);
 int read_device_fault(int* fault, cudaStream_t stream);
@@ -62,9 +62,14 @@ int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq,
   return mmvq::launch_quantize_q8_1(x, K, ncols, ldx, xq, (cudaStream_t)stream);
 }
 
+static bool dense_type(int type) {
+  return type == MMVQ_Q4_K || type == MMVQ_Q6_K || type == MMVQ_Q4_K_PLANAR ||
+         type == MMVQ_Q6_K_PLANAR;
+}
+
 static int gemv_checks(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
                        const void* out) {
-  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K && type != MMVQ_Q6_K_PLANAR) return MMVQ_ERR_TYPE;
+  if (!dense_type(type)) return MMVQ_ERR_TYPE;
   if (!W || !xq || !out) return MMVQ_ERR_NULL;
   const int rc = check_weights_shape(rows, K);
   if (rc) return rc;
@@ -101,10 +106,11 @@ int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, i
                  const int32_t* expert_ids, const int32_t* token_offsets, int n_groups,
                  const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
                  int32_t* status, mmvq_stream_t stream) {
-  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K) return MMVQ_ERR_TYPE;
+  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K && type != MMVQ_Q4_K_PLANAR) return MMVQ_ERR_TYPE;
   if (!W_experts || !expert_ids || !token_offsets || !xq || !y) return MMVQ_ERR_NULL;
   int rc = check_weights_shape(rows, K);
   if (rc) return rc;
+  if (type == MMVQ_Q4_K_PLANAR && rows % mmvq::kTileRows != 0) return MMVQ_ERR_SHAPE;
   if (n_experts < 1 || n_xq_cols < 1) return MMVQ_ERR_SHAPE;
   if (n_groups < 1 || n_groups > 4096) return MMVQ_ERR_ROUTING;
   if (!aligned(W_experts, 16) || !aligned(xq, 16) || !aligned(y, 4) || !aligned(expert_ids, 4) ||
@@ -137,20 +143,21 @@ int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq, float* 
   return mmvq::launch_silu_mul_quantize(gu, F, n, xq, h_out, (cudaStream_t)stream);
 }
 
-int64_t mmvq_planar_bytes(int64_t rows, int K) {
+int64_t mmvq_planar_bytes(int type, int64_t rows, int K) {
+  if (type != MMVQ_Q6_K && type != MMVQ_Q4_K) return -1;
   if (check_weights_shape(rows, K) != MMVQ_OK) return -1;
   const int64_t groups = (rows + mmvq::kTileRows - 1) / mmvq::kTileRows;
-  return groups * (K / mmvq::kQK) * mmvq::kTileBytes;
+  return groups * (K / mmvq::kQK) * (type == MMVQ_Q4_K ? mmvq::kTileBytesQ4 : mmvq::kTileBytes);
 }
 
 int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int K, void* W_planar,
                        mmvq_stream_t stream) {
-  if (type != MMVQ_Q6_K) return MMVQ_ERR_TYPE;
+  if (type != MMVQ_Q6_K && type != MMVQ_Q4_K) return MMVQ_ERR_TYPE;
   if (!W_gguf || !W_planar) return MMVQ_ERR_NULL;
   const int rc = check_weights_shape(rows, K);
   if (rc) return rc;
-  if (!aligned(W_gguf, 2) || !aligned(W_planar, 16)) return MMVQ_ERR_ALIGN;
-  return mmvq::launch_repack_planar(W_gguf, rows, K, W_planar, (cudaStream_t)stream);
+  if (!aligned(W_gguf, type == MMVQ_Q4_K ? 16 : 2) || !aligned(W_planar, 16)) return MMVQ_ERR_ALIGN;
+  return mmvq::launch_repack_planar(type, W_gguf, rows, K, W_planar, (cudaStream_t)stream);
 }
 
 int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int32_t* row_ids,
@@ -167,7 +174,7 @@ int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int
 }
 
 int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
-  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K && type != MMVQ_Q6_K_PLANAR) return MMVQ_ERR_TYPE;
+  if (!dense_type(type)) return MMVQ_ERR_TYPE;
   if (!info) return MMVQ_ERR_NULL;
   const int rc = check_weights_shape(rows, K);
   if (rc) return rc;

@@ -275,6 +275,42 @@ __device__ __forceinline__ void load_q4_gguf(const uint8_t* __restrict__ blk, in
   }
 }
 
+// Planar Q4_K tile in global memory (2304 bytes): lane L reads qs chunks
+// [512j + 16L] and its row's header at [2048 + 16i].
+__device__ __forceinline__ void load_q4_planar(const uint8_t* __restrict__ tile, int lane,
+                                               Q4Half& w) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 v = ldg_nc_v4(tile + 512 * j + 16 * lane);
+    w.qs[4 * j + 0] = v.x;
+    w.qs[4 * j + 1] = v.y;
+    w.qs[4 * j + 2] = v.z;
+    w.qs[4 * j + 3] = v.w;
+  }
+  const uint4 hv = ldg_nc_v4(tile + 2048 + 16 * (lane & 15));
+  w.hdr[0] = hv.x;
+  w.hdr[1] = hv.y;
+  w.hdr[2] = hv.z;
+  w.hdr[3] = hv.w;
+}
+
+// The same tile staged in shared memory.
+__device__ __forceinline__ void load_q4_tile_smem(const uint8_t* tile, int lane, Q4Half& w) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + 512 * j + 16 * lane);
+    w.qs[4 * j + 0] = v.x;
+    w.qs[4 * j + 1] = v.y;
+    w.qs[4 * j + 2] = v.z;
+    w.qs[4 * j + 3] = v.w;
+  }
+  const uint4 hv = *reinterpret_cast<const uint4*>(tile + 2048 + 16 * (lane & 15));
+  w.hdr[0] = hv.x;
+  w.hdr[1] = hv.y;
+  w.hdr[2] = hv.z;
+  w.hdr[3] = hv.w;
+}
+
 __device__ __forceinline__ uint32_t byte_of(const uint32_t (&hdr)[4], int k) {
   // byte k (0..15) of the header; k is a compile-time constant after unrolling
   return (hdr[k >> 2] >> (8 * (k & 3))) & 0xffu;

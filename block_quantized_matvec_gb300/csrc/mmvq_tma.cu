@@ -1,4 +1,4 @@
-// Planar Q6_K MMVQ fed by bulk copies (cp.async.bulk, the 1-D TMA path) into
+// Planar (Q6_K and Q4_K tile) MMVQ fed by bulk copies (cp.async.bulk, the 1-D TMA path) into
 // a shared-memory ring ("Strata" PR #2340 "STRATA_Q6_PLANAR": the head's
 // planes are laid out so every lane load is one aligned 16-byte load; PR
 // #2207: the weights are read once for all 1-8 columns).
@@ -118,10 +118,14 @@ __device__ __forceinline__ void load_q6_tile_smem(const uint8_t* tile, int lane,
 // (S stages of G*P tiles, 128-byte aligned), the activation quants, d_a as
 // floats, the K-slice partials [C][8][16].
 __host__ __device__ inline size_t tma_ring_offset(int S) { return ((size_t)16 * S + 16 + 127) & ~size_t(127); }
-__host__ __device__ inline size_t tma_smem_bytes(int S, int K, int ncols, int G, int P) {
+__host__ __device__ constexpr int tile_bytes(int layout) {
+  return layout == kQ4Planar ? kTileBytesQ4 : kTileBytes;
+}
+__host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int ncols, int G, int P) {
   const int C = G * P;
-  return tma_ring_offset(S) + (size_t)S * C * kTileBytes + (size_t)ncols * act_row_bytes(K) +
-         (size_t)ncols * (K / kQK8) * 4 + (size_t)C * kMaxCols * kTileRows * 4;
+  return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + (size_t)ncols * act_row_bytes(K) +
+         (size_t)ncols * (K / kQK8) * 4 * (layout == kQ4Planar ? 2 : 1) +
+         (size_t)C * kMaxCols * kTileRows * 4;
 }
 
 __device__ __forceinline__ void group_sync(int id, int nthreads) {
@@ -133,8 +137,8 @@ __device__ __forceinline__ void group_sync(int id, int nthreads) {
 // batch, stage bb holds, for each group, the P consecutive tiles
 // bb*P .. bb*P+P-1 of its row group, and warp (g, p) takes tile bb*P+p.  The
 // P partial sums of a row group are added in warp order at the batch end.
-template <int NCOLS>
-__global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __restrict__ W,
+template <int LAYOUT, int NCOLS>
+__global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t* __restrict__ W,
                                                                int64_t rows, int K,
                                                                const uint8_t* __restrict__ xq,
                                                                float* __restrict__ y,
@@ -148,8 +152,9 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
   const int nbq = K / kQK8;
   const int rb = act_row_bytes(K);
   const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
+  constexpr int TB = tile_bytes(LAYOUT);
   const int spb = nb / P;  // stages per batch
-  const size_t stage_bytes = (size_t)C * kTileBytes;
+  const size_t stage_bytes = (size_t)C * TB;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + S;
@@ -157,7 +162,8 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
   uint8_t* ring = smem + tma_ring_offset(S);
   uint8_t* act = ring + (size_t)S * stage_bytes;
   float* da = reinterpret_cast<float*>(act + NCOLS * rb);
-  float* red = da + NCOLS * nbq;
+  float* sa = da + NCOLS * nbq;  // Q4_K only
+  float* red = sa + (LAYOUT == kQ4Planar ? NCOLS * nbq : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -190,12 +196,11 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
         const int bb = (int)(it % spb);
         const int64_t left = my_rgs - j * G;
         const int valid = (int)(left < G ? left : G);
-        mbar_expect_tx(&full[s], (uint32_t)(valid * P * kTileBytes));
+        mbar_expect_tx(&full[s], (uint32_t)(valid * P * TB));
         for (int g = 0; g < valid; ++g) {
           const int64_t rg = blockIdx.x + (j * G + g) * (int64_t)gridDim.x;
-          bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)g * P * kTileBytes,
-                   W + (rg * nb + (int64_t)bb * P) * kTileBytes, (uint32_t)(P * kTileBytes),
-                   &full[s]);
+          bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)g * P * TB,
+                   W + (rg * nb + (int64_t)bb * P) * TB, (uint32_t)(P * TB), &full[s]);
         }
       }
       // no copy of this CTA may land after it exits: wait (bounded) for the
@@ -218,7 +223,8 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
   const bool stable = (flags & MMVQ_FLAG_XQ_STABLE) != 0;
   bool waited = !stable;
   if (!stable) grid_dependency_wait();
-  stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da, nullptr, tid, nthreads);
+  stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da,
+             LAYOUT == kQ4Planar ? sa : nullptr, tid, nthreads);
   group_sync(1, nthreads);
 
   const int g = warp / P;
@@ -245,11 +251,20 @@ __global__ void __launch_bounds__(13 * 32) mmvq_q6p_tma_kernel(const uint8_t* __
         *fail = 1;
         atomicOr(&g_fault_word, kFaultMbarTimeout);
       }
-      Q6Half w;
-      if (valid) load_q6_tile_smem(ring + (size_t)s * stage_bytes + (size_t)warp * kTileBytes, lane, w);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (valid) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, rows * nbq);
+      const uint8_t* tile = ring + (size_t)s * stage_bytes + (size_t)warp * TB;
+      if (LAYOUT == kQ4Planar) {
+        Q4Half w;
+        if (valid) load_q4_tile_smem(tile, lane, w);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (valid) q4_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, rows * nbq);
+      } else {
+        Q6Half w;
+        if (valid) load_q6_tile_smem(tile, lane, w);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (valid) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, rows * nbq);
+      }
     }
     // halves of each row, then the group's K-slices in warp order
 #pragma unroll
@@ -295,7 +310,7 @@ struct TmaCfg {
 // per batch, each stage one tile per consumer warp; the SM's issue rate is
 // shared by all resident consumer warps.  The cheapest shape wins; ties go
 // to more consumer warps.
-template <int NCOLS>
+template <int LAYOUT, int NCOLS>
 static int tma_config(int64_t rows, int K, TmaCfg* out) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, TmaCfg> cache;
@@ -309,7 +324,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
       return MMVQ_OK;
     }
   }
-  auto kern = mmvq_q6p_tma_kernel<NCOLS>;
+  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS>;
   const int sms = device_sms();
   const size_t limit = max_smem_optin();
   if (sms <= 0 || limit == 0) return MMVQ_ERR_CUDA;
@@ -319,13 +334,33 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
   TmaCfg best = {0, 0, 0, 0, 0};
   double best_cost = 1e300;
   int best_c = 0;
-  for (int P = 1; P <= std::min(nb, 12); ++P) {
+  // Very tall matrices (an LM head): one warp per row group (no K-split, no
+  // barriers), seven row groups per CTA, a two-stage ring, so that three
+  // CTAs (21 consumer warps) share each SM.  Measured on GB300: ~15% faster
+  // than the split-K shapes for 151936 x 2560.
+  const bool tall = n_rg >= (int64_t)16 * sms;
+  if (tall) {
+    for (int G = 7; G >= 1 && best.G == 0; --G) {
+      const size_t smem = tma_smem_bytes(LAYOUT, 2, K, NCOLS, G, 1);
+      if (smem > limit) continue;
+      if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (G + 1), smem) !=
+          cudaSuccess)
+        return MMVQ_ERR_CUDA;
+      if (per_sm < 1) continue;
+      const int64_t ctas = std::min<int64_t>((n_rg + G - 1) / G, (int64_t)sms * per_sm);
+      best = {G, 1, 2, (int)ctas, smem};
+    }
+  }
+  const bool search = !tall || best.G == 0;
+  for (int P = 1; P <= std::min(nb, 12) && search; ++P) {
     if (nb % P) continue;
     for (int G = 1; G * P <= 12; ++G) {
       int S = 0;
       size_t smem = 0;
       for (int s = 32; s >= 2; --s) {
-        const size_t b = tma_smem_bytes(s, K, NCOLS, G, P);
+        const size_t b = tma_smem_bytes(LAYOUT, s, K, NCOLS, G, P);
         if (b <= budget || (s == 2 && b <= limit)) {
           S = s;
           smem = b;
@@ -361,37 +396,46 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
   return MMVQ_OK;
 }
 
-template <int NCOLS>
+template <int LAYOUT, int NCOLS>
 static int launch_tma_t(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
                         int32_t* sumi, uint32_t flags, cudaStream_t stream) {
   TmaCfg cfg;
-  const int rc = tma_config<NCOLS>(rows, K, &cfg);
+  const int rc = tma_config<LAYOUT, NCOLS>(rows, K, &cfg);
   if (rc != MMVQ_OK) return rc;
-  return launch_pdl(mmvq_q6p_tma_kernel<NCOLS>, dim3(cfg.grid), dim3(32 * (cfg.G * cfg.P + 1)),
-                    cfg.smem, stream, W, rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, flags);
+  return launch_pdl(mmvq_planar_tma_kernel<LAYOUT, NCOLS>, dim3(cfg.grid),
+                    dim3(32 * (cfg.G * cfg.P + 1)), cfg.smem, stream, W, rows, K, xq, y, sumi,
+                    cfg.slots, cfg.G, cfg.P, flags);
 }
 
-int launch_q6_planar_tma(const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
-                         int32_t* sumi, uint32_t flags, cudaStream_t s) {
-  const uint8_t* w = static_cast<const uint8_t*>(W);
-  const uint8_t* x = static_cast<const uint8_t*>(xq);
+template <int LAYOUT>
+static int launch_tma_layout(const uint8_t* w, int64_t rows, int K, const uint8_t* x, int ncols,
+                             float* y, int32_t* sumi, uint32_t flags, cudaStream_t s) {
   switch (ncols) {
-    case 1: return launch_tma_t<1>(w, rows, K, x, y, sumi, flags, s);
-    case 2: return launch_tma_t<2>(w, rows, K, x, y, sumi, flags, s);
-    case 3: return launch_tma_t<3>(w, rows, K, x, y, sumi, flags, s);
-    case 4: return launch_tma_t<4>(w, rows, K, x, y, sumi, flags, s);
-    case 5: return launch_tma_t<5>(w, rows, K, x, y, sumi, flags, s);
-    case 6: return launch_tma_t<6>(w, rows, K, x, y, sumi, flags, s);
-    case 7: return launch_tma_t<7>(w, rows, K, x, y, sumi, flags, s);
-    case 8: return launch_tma_t<8>(w, rows, K, x, y, sumi, flags, s);
+    case 1: return launch_tma_t<LAYOUT, 1>(w, rows, K, x, y, sumi, flags, s);
+    case 2: return launch_tma_t<LAYOUT, 2>(w, rows, K, x, y, sumi, flags, s);
+    case 3: return launch_tma_t<LAYOUT, 3>(w, rows, K, x, y, sumi, flags, s);
+    case 4: return launch_tma_t<LAYOUT, 4>(w, rows, K, x, y, sumi, flags, s);
+    case 5: return launch_tma_t<LAYOUT, 5>(w, rows, K, x, y, sumi, flags, s);
+    case 6: return launch_tma_t<LAYOUT, 6>(w, rows, K, x, y, sumi, flags, s);
+    case 7: return launch_tma_t<LAYOUT, 7>(w, rows, K, x, y, sumi, flags, s);
+    case 8: return launch_tma_t<LAYOUT, 8>(w, rows, K, x, y, sumi, flags, s);
   }
   return MMVQ_ERR_NCOLS;
 }
 
-template <int NCOLS>
+int launch_planar_tma(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
+                      float* y, int32_t* sumi, uint32_t flags, cudaStream_t s) {
+  const uint8_t* w = static_cast<const uint8_t*>(W);
+  const uint8_t* x = static_cast<const uint8_t*>(xq);
+  if (type == MMVQ_Q4_K_PLANAR)
+    return launch_tma_layout<kQ4Planar>(w, rows, K, x, ncols, y, sumi, flags, s);
+  return launch_tma_layout<kQ6Planar>(w, rows, K, x, ncols, y, sumi, flags, s);
+}
+
+template <int LAYOUT, int NCOLS>
 static int tma_shape_t(int64_t rows, int K, int32_t* info) {
   TmaCfg cfg;
-  const int rc = tma_config<NCOLS>(rows, K, &cfg);
+  const int rc = tma_config<LAYOUT, NCOLS>(rows, K, &cfg);
   if (rc != MMVQ_OK) return rc;
   info[0] = cfg.grid;
   info[1] = 32 * (cfg.G * cfg.P + 1);
@@ -402,18 +446,24 @@ static int tma_shape_t(int64_t rows, int K, int32_t* info) {
   return MMVQ_OK;
 }
 
-int q6_planar_tma_shape(int64_t rows, int K, int ncols, int32_t* info) {
+template <int LAYOUT>
+static int tma_shape_layout(int64_t rows, int K, int ncols, int32_t* info) {
   switch (ncols) {
-    case 1: return tma_shape_t<1>(rows, K, info);
-    case 2: return tma_shape_t<2>(rows, K, info);
-    case 3: return tma_shape_t<3>(rows, K, info);
-    case 4: return tma_shape_t<4>(rows, K, info);
-    case 5: return tma_shape_t<5>(rows, K, info);
-    case 6: return tma_shape_t<6>(rows, K, info);
-    case 7: return tma_shape_t<7>(rows, K, info);
-    case 8: return tma_shape_t<8>(rows, K, info);
+    case 1: return tma_shape_t<LAYOUT, 1>(rows, K, info);
+    case 2: return tma_shape_t<LAYOUT, 2>(rows, K, info);
+    case 3: return tma_shape_t<LAYOUT, 3>(rows, K, info);
+    case 4: return tma_shape_t<LAYOUT, 4>(rows, K, info);
+    case 5: return tma_shape_t<LAYOUT, 5>(rows, K, info);
+    case 6: return tma_shape_t<LAYOUT, 6>(rows, K, info);
+    case 7: return tma_shape_t<LAYOUT, 7>(rows, K, info);
+    case 8: return tma_shape_t<LAYOUT, 8>(rows, K, info);
   }
   return MMVQ_ERR_NCOLS;
+}
+
+int planar_tma_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
+  if (type == MMVQ_Q4_K_PLANAR) return tma_shape_layout<kQ4Planar>(rows, K, ncols, info);
+  return tma_shape_layout<kQ6Planar>(rows, K, ncols, info);
 }
 
 // Reads and clears the device fault word (after synchronising `stream`).

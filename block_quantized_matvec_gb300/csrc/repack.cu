@@ -72,6 +72,34 @@ __global__ void __launch_bounds__(256) repack_planar_kernel(const uint8_t* __res
   *reinterpret_cast<uint4*>(P + t * kTileBytes + 16 * q) = *reinterpret_cast<const uint4*>(buf);
 }
 
+// Planar Q4_K: one CTA per tile; thread q < 144 writes 16-byte chunk q
+// (q < 128: qs[64u + 16j] of lane L = q % 32, j = q / 32; else the header
+// of row q - 128).  Q4_K blocks are 16-byte aligned, so reads are uint4.
+__global__ void __launch_bounds__(256) repack_planar_q4_kernel(const uint8_t* __restrict__ W,
+                                                               int64_t rows, int nb,
+                                                               uint8_t* __restrict__ P) {
+  // Writes weights: no early launch of the next kernel.
+  grid_dependency_wait();
+  const int64_t t = blockIdx.x;
+  const int64_t g = t / nb;
+  const int b = (int)(t - g * nb);
+  const int q = threadIdx.x;
+  if (q >= kTileBytesQ4 / 16) return;
+  int i, off;
+  if (q < 128) {
+    const int j = q >> 5, L = q & 31;
+    i = L & 15;
+    off = 16 + 64 * (L >> 4) + 16 * j;
+  } else {
+    i = q - 128;
+    off = 0;
+  }
+  const int64_t row = g * kTileRows + i;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (row < rows) v = *reinterpret_cast<const uint4*>(W + (row * nb + b) * kQ4KBytes + off);
+  *reinterpret_cast<uint4*>(P + t * kTileBytesQ4 + 16 * q) = v;
+}
+
 // One CTA per output tile; out row k = source row row_ids[k] (zero bytes
 // for k >= n or an invalid id).
 __global__ void __launch_bounds__(256) gather_planar_kernel(const uint8_t* __restrict__ P,
@@ -221,10 +249,13 @@ __global__ void __launch_bounds__(1024) route_groups_kernel(const int32_t* __res
   }
 }
 
-int launch_repack_planar(const void* W, int64_t rows, int K, void* P, cudaStream_t s) {
+int launch_repack_planar(int type, const void* W, int64_t rows, int K, void* P, cudaStream_t s) {
   const int nb = K / kQK;
   const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * nb;
   if (tiles > 0x7fffffff) return MMVQ_ERR_SHAPE;
+  if (type == MMVQ_Q4_K)
+    return launch_pdl(repack_planar_q4_kernel, dim3((unsigned)tiles), dim3(256), 0, s,
+                      static_cast<const uint8_t*>(W), rows, nb, static_cast<uint8_t*>(P));
   return launch_pdl(repack_planar_kernel, dim3((unsigned)tiles), dim3(256), 0, s,
                     static_cast<const uint8_t*>(W), rows, nb, static_cast<uint8_t*>(P));
 }

@@ -8,8 +8,6 @@
 
 namespace mmvq {
 
-enum Layout { kQ6Planar = 0, kQ6Gguf = 1, kQ4Gguf = 2 };
-
 constexpr int kGgufSlot = 224;                     // 14 aligned 16-byte chunks per Q6_K block
 constexpr int kGgufStage = kTileRows * kGgufSlot;  // one warp, one block step
 
@@ -94,6 +92,17 @@ __device__ __forceinline__ void rowgroup_dot(const uint8_t* __restrict__ W, int6
       q6_dot<NC>(cur, h, b, act, rb, da, nbq, acc, srow, scs);
       slot ^= 1;
     }
+  } else if (LAYOUT == kQ4Planar) {
+    const uint8_t* tiles = W + (size_t)rg * nb * kTileBytesQ4;
+    int b = wk;
+    Q4Half cur;
+    if (b < nb) load_q4_planar(tiles + (size_t)b * kTileBytesQ4, lane, cur);
+    for (; b < nb; b += WK) {
+      Q4Half nxt;
+      if (b + WK < nb) load_q4_planar(tiles + (size_t)(b + WK) * kTileBytesQ4, lane, nxt);
+      q4_dot<NC>(cur, h, b, act, rb, da, sa, nbq, acc, srow, scs);
+      cur = nxt;
+    }
   } else {
     const int64_t rr = min(row, rows - 1);
     const uint8_t* wrow = W + (size_t)rr * nb * kQ4KBytes;
@@ -147,7 +156,7 @@ __device__ __forceinline__ void reduce_store(float (&acc)[NC], int lane, int wk,
 // Dynamic shared memory of a CTA with `nwarps` warps and `ncols` staged columns.
 __host__ __device__ inline size_t mmvq_smem_bytes(int layout, int K, int ncols, int nwarps) {
   size_t s = (size_t)ncols * act_row_bytes(K);                            // quants
-  s += (size_t)ncols * (K / kQK8) * 4 * (layout == kQ4Gguf ? 2 : 1);      // d (and s)
+  s += (size_t)ncols * (K / kQK8) * 4 * ((layout == kQ4Gguf || layout == kQ4Planar) ? 2 : 1);
   s += (size_t)nwarps * kMaxCols * kTileRows * 4;                          // K-slice partials
   if (layout == kQ6Gguf) s += (size_t)nwarps * 2 * kGgufStage;             // cp.async ring
   return s;

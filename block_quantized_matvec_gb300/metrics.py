@@ -8,7 +8,8 @@ bytes of the distinct experts actually read.
 """
 from __future__ import annotations
 
-BYTES_PER_256 = {"q6_k": 210, "q6_k_planar": 210, "q4_k": 144, "iq3_s": 110}
+BYTES_PER_256 = {"q6_k": 210, "q6_k_planar": 210, "q6_k_planar_draft": 210, "q4_k": 144,
+                 "q4_k_planar": 144, "iq3_s": 110}
 Q8_1_BYTES_PER_32 = 36
 
 
@@ -26,3 +27,9 @@ def call_bytes(fmt: str, rows: int, K: int, ncols: int) -> int:
 
 def gbps(nbytes: float, seconds: float) -> float:
     return nbytes / seconds / 1e9
+
+
+def moe_step_bytes(distinct_experts: int, hidden: int, ffn: int, fmt: str = "q4_k") -> int:
+    """Weight bytes one MoE step reads: every distinct routed expert's gate|up
+    (2*ffn x hidden) and down (hidden x ffn) matrices, once."""
+    return distinct_experts * (weight_bytes(fmt, 2 * ffn, hidden) + weight_bytes(fmt, hidden, ffn))

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libmmvq.so")
 TYPE_Q4_K = 12
 TYPE_Q6_K = 14
 TYPE_Q6_K_PLANAR = 1014
-BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210, TYPE_Q6_K_PLANAR: 210}
+TYPE_Q4_K_PLANAR = 1012
+BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210, TYPE_Q6_K_PLANAR: 210, TYPE_Q4_K_PLANAR: 144}
 Q8_1_BYTES = 36
 MAX_COLS = 8
 
@@ -39,7 +40,7 @@ SIGNATURES = {
     "mmvq_grouped": (_I, [_I, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P]),
     "mmvq_route_groups": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "mmvq_silu_mul_quantize_q8_1": (_I, [_P, _I, _I, _P, _P, _P]),
-    "mmvq_planar_bytes": (_I64, [_I64, _I]),
+    "mmvq_planar_bytes": (_I64, [_I, _I64, _I]),
     "mmvq_repack_planar": (_I, [_I, _P, _I64, _I, _P, _P]),
     "mmvq_gather_planar_rows": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P]),
     "mmvq_read_device_fault": (_I, [_P, _P]),
@@ -195,7 +196,8 @@ def launch_shape(type_: int, rows: int, K: int, ncols: int) -> dict:
     """The launch shape mmvq_gemv picks (host-only query)."""
     info = (ctypes.c_int32 * 6)()
     _check(lib().mmvq_launch_shape(type_, rows, K, ncols, info), "mmvq_launch_shape")
-    keys = (["grid", "threads", "smem", "G", "P", "stages"] if type_ == TYPE_Q6_K_PLANAR
+    keys = (["grid", "threads", "smem", "G", "P", "stages"]
+            if type_ in (TYPE_Q6_K_PLANAR, TYPE_Q4_K_PLANAR)
             else ["grid", "threads", "smem", "WR", "WK", "unused"])
     return dict(zip(keys, list(info)))
 
@@ -207,20 +209,20 @@ def read_device_fault(stream=None) -> int:
     return v.value
 
 
-def planar_bytes(rows: int, K: int) -> int:
-    n = lib().mmvq_planar_bytes(rows, K)
+def planar_bytes(rows: int, K: int, type_: int = TYPE_Q6_K) -> int:
+    n = lib().mmvq_planar_bytes(type_, rows, K)
     if n < 0:
         raise MMVQError(ERR_SHAPE, "mmvq_planar_bytes")
     return int(n)
 
 
 def repack_planar(W_gguf: torch.Tensor, rows: int, K: int, out: torch.Tensor | None = None,
-                  stream=None) -> torch.Tensor:
-    """GGUF Q6_K bytes -> planar tiles (uint8, planar_bytes(rows, K))."""
+                  stream=None, type_: int = TYPE_Q6_K) -> torch.Tensor:
+    """GGUF Q6_K (or Q4_K) bytes -> planar tiles (uint8, planar_bytes(rows, K, type_))."""
     _dev(W_gguf, "W_gguf")
     if out is None:
-        out = torch.empty(planar_bytes(rows, K), dtype=torch.uint8, device=W_gguf.device)
-    _check(lib().mmvq_repack_planar(TYPE_Q6_K, _ptr(W_gguf), rows, K, _ptr(out), _stream(stream)),
+        out = torch.empty(planar_bytes(rows, K, type_), dtype=torch.uint8, device=W_gguf.device)
+    _check(lib().mmvq_repack_planar(type_, _ptr(W_gguf), rows, K, _ptr(out), _stream(stream)),
            "mmvq_repack_planar")
     return out
 

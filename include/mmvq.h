@@ -44,7 +44,13 @@
  *      bytes [3072 + 8*L, +8)                     : scales[8*h .. 8*h+7]
  *      bytes [3328 + 2*i, +2)                     : d
  *    so each warp-wide 16-byte load reads one contiguous 512-byte segment.
- *    Size: mmvq_planar_bytes(rows, K).
+ *    Size: mmvq_planar_bytes(MMVQ_Q6_K, rows, K).
+ *  - Planar Q4_K (MMVQ_Q4_K_PLANAR), the same idea for Q4_K: 2304-byte
+ *    tiles T(g, b) in the same order; lane L = 16*u + i (u = half of the
+ *    block, i.e. sub-blocks 4u..4u+3):
+ *      bytes [512*j + 16*L, +16)  j = 0..3 : qs[64*u + 16*j .. +15]
+ *      bytes [2048 + 16*i, +16)            : d, dmin, scales[12] of row i
+ *    Size: mmvq_planar_bytes(MMVQ_Q4_K, rows, K).
  *
  * Results: y is fp32, [ncols][rows] (column-major over the activation
  * columns).  Block sums are exact integers; the FP32 output of a row is
@@ -72,9 +78,10 @@ typedef struct CUstream_st* mmvq_stream_t; /* == cudaStream_t */
 #endif
 
 enum mmvq_type {
-  MMVQ_Q4_K = 12,         /* GGUF Q4_K blocks, 144 B / 256 weights */
-  MMVQ_Q6_K = 14,         /* GGUF Q6_K blocks, 210 B / 256 weights */
-  MMVQ_Q6_K_PLANAR = 1014 /* Q6_K in 16-row planar tiles (see above) */
+  MMVQ_Q4_K = 12,          /* GGUF Q4_K blocks, 144 B / 256 weights */
+  MMVQ_Q6_K = 14,          /* GGUF Q6_K blocks, 210 B / 256 weights */
+  MMVQ_Q4_K_PLANAR = 1012, /* Q4_K in 16-row planar tiles (see above) */
+  MMVQ_Q6_K_PLANAR = 1014  /* Q6_K in 16-row planar tiles (see above) */
 };
 
 /* Flags of mmvq_gemv_ex. */
@@ -119,7 +126,7 @@ MMVQ_API int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, v
 /*
  * Dense MMVQ (PR #2207 wide kernels, PR #1774 iq3s_wide_kernel: weights read
  * once for all 1-8 columns).  W: rows x K/256 blocks of `type` (MMVQ_Q4_K,
- * MMVQ_Q6_K or MMVQ_Q6_K_PLANAR); xq: [ncols][K/32] Q8_1 blocks;
+ * MMVQ_Q6_K, MMVQ_Q4_K_PLANAR or MMVQ_Q6_K_PLANAR); xq: [ncols][K/32] Q8_1 blocks;
  * y: fp32 [ncols][rows].  Requires K % 256 == 0 (PR #1774: the row length a
  * multiple of 256), 1 <= ncols <= 8 (PR #2207: 1 to 8 columns),
  * K <= 16384, 1 <= rows <= 2^31 - 1.
@@ -152,8 +159,9 @@ MMVQ_API int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K,
 /*
  * Grouped expert MMVQ over per-expert token lists (PR #2746 "B70
  * validation": grouped calls with empty groups; issue #2801: the grouped
- * gate/up and down kernels).  W_experts: [n_experts][rows][K/256] blocks of
- * `type` (MMVQ_Q4_K or MMVQ_Q6_K).  Group g (0 <= g < n_groups) multiplies
+ * gate/up and down kernels).  W_experts: n_experts matrices of rows x K,
+ * one after another, of `type` (MMVQ_Q4_K, MMVQ_Q6_K, or MMVQ_Q4_K_PLANAR
+ * with each expert repacked on its own, rows a multiple of 16).  Group g (0 <= g < n_groups) multiplies
  * expert expert_ids[g] with the activation columns of positions
  * p in [token_offsets[g], token_offsets[g+1]); column act_index[p] of xq
  * (column p when act_index == NULL).  Output row p: y[p][0..rows).
@@ -193,14 +201,16 @@ MMVQ_API int mmvq_route_groups(const int32_t* topk, int T, int k, int n_experts,
 MMVQ_API int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq, float* h_out,
                                 mmvq_stream_t stream);
 
-/* Bytes of the planar Q6_K form of a rows x K matrix; -1 on bad shape. */
-MMVQ_API int64_t mmvq_planar_bytes(int64_t rows, int K);
+/* Bytes of the planar form of a rows x K matrix of `type` (MMVQ_Q6_K or
+ * MMVQ_Q4_K); -1 on a bad type or shape. */
+MMVQ_API int64_t mmvq_planar_bytes(int type, int64_t rows, int K);
 
 /*
  * Load-time repack of GGUF Q6_K blocks into planar tiles (PR #2340
  * "STRATA_Q6_PLANAR": same bytes, the GGUF copy can then be freed).
- * Out-of-place; W_planar holds mmvq_planar_bytes(rows, K) bytes; pad rows
- * are written as zeros.  type must be MMVQ_Q6_K.  K % 256 == 0.
+ * Out-of-place; W_planar holds mmvq_planar_bytes(type, rows, K) bytes; pad
+ * rows are written as zeros.  type: MMVQ_Q6_K (-> MMVQ_Q6_K_PLANAR) or
+ * MMVQ_Q4_K (-> MMVQ_Q4_K_PLANAR).  K % 256 == 0.
  */
 MMVQ_API int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int K, void* W_planar,
                        mmvq_stream_t stream);
@@ -209,7 +219,7 @@ MMVQ_API int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int 
  * Draft-head gather (PR #2340: "the draft head's subset is gathered from the
  * planar head"): out = planar matrix of n rows whose row k is row
  * row_ids[k] of the planar matrix W_planar (rows x K).  out holds
- * mmvq_planar_bytes(n, K) bytes.  Row ids outside [0, rows) give zero rows
+ * mmvq_planar_bytes(MMVQ_Q6_K, n, K) bytes.  Row ids outside [0, rows) give zero rows
  * and set *status to MMVQ_ERR_ROUTING when status != NULL.
  */
 MMVQ_API int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int32_t* row_ids,

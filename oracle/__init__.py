@@ -27,6 +27,7 @@ _lib = None
 TYPE_Q4_K = 12
 TYPE_Q6_K = 14
 TYPE_Q6_K_PLANAR = 1014
+TYPE_Q4_K_PLANAR = 1012
 
 Q81_BYTES = 36
 BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210}
@@ -59,6 +60,10 @@ def _load():
             lib.orc_decode_q4_k.argtypes = [P, P, P, P, P, P]
             lib.orc_planar_bytes.argtypes = [I64, I]
             lib.orc_planar_bytes.restype = I64
+            lib.orc_planar_bytes_q4.argtypes = [I64, I]
+            lib.orc_planar_bytes_q4.restype = I64
+            lib.orc_repack_planar_q4.argtypes = [P, I64, I, P]
+            lib.orc_unpack_planar_q4.argtypes = [P, I64, I, P]
             lib.orc_repack_planar.argtypes = [P, I64, I, P]
             lib.orc_unpack_planar.argtypes = [P, I64, I, P]
             lib.orc_gather_planar_rows.argtypes = [P, I64, I, P, I, P]
@@ -131,21 +136,27 @@ def decode_q4_k(block: np.ndarray):
     return q, sc, m, float(d[0]), float(dmin[0])
 
 
-def planar_bytes(rows: int, K: int) -> int:
+def planar_bytes(rows: int, K: int, type_: int = TYPE_Q6_K) -> int:
+    if type_ == TYPE_Q4_K:
+        return int(_load().orc_planar_bytes_q4(rows, K))
     return int(_load().orc_planar_bytes(rows, K))
 
 
-def repack_planar(W: np.ndarray, rows: int, K: int) -> np.ndarray:
+def repack_planar(W: np.ndarray, rows: int, K: int, type_: int = TYPE_Q6_K) -> np.ndarray:
+    """GGUF blocks of type_ (Q6_K or Q4_K) -> planar tiles."""
     W = np.ascontiguousarray(W, dtype=np.uint8)
-    out = np.empty(planar_bytes(rows, K), dtype=np.uint8)
-    _check(_load().orc_repack_planar(_p(W), rows, K, _p(out)), "repack_planar")
+    out = np.empty(planar_bytes(rows, K, type_), dtype=np.uint8)
+    fn = _load().orc_repack_planar_q4 if type_ == TYPE_Q4_K else _load().orc_repack_planar
+    _check(fn(_p(W), rows, K, _p(out)), "repack_planar")
     return out
 
 
-def unpack_planar(P: np.ndarray, rows: int, K: int) -> np.ndarray:
+def unpack_planar(P: np.ndarray, rows: int, K: int, type_: int = TYPE_Q6_K) -> np.ndarray:
     P = np.ascontiguousarray(P, dtype=np.uint8)
-    out = np.empty((rows, K // 256, 210), dtype=np.uint8)
-    _check(_load().orc_unpack_planar(_p(P), rows, K, _p(out)), "unpack_planar")
+    bb = 144 if type_ == TYPE_Q4_K else 210
+    out = np.empty((rows, K // 256, bb), dtype=np.uint8)
+    fn = _load().orc_unpack_planar_q4 if type_ == TYPE_Q4_K else _load().orc_unpack_planar
+    _check(fn(_p(P), rows, K, _p(out)), "unpack_planar")
     return out
 
 

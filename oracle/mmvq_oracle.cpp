@@ -59,10 +59,12 @@ const int kQ4KBytes = 144;  // d dmin scales[12] qs[128]
 const int kTypeQ4K = 12;
 const int kTypeQ6K = 14;
 const int kTypeQ6KPlanar = 1014;
+const int kTypeQ4KPlanar = 1012;
 
 // Planar tile: 16 rows x one 256-block.
 const int kTileRows = 16;
-const int kTileBytes = 3360;
+const int kTileBytes = 3360;     // Q6_K
+const int kTileBytesQ4 = 2304;   // Q4_K
 
 // ---------------------------------------------------------------- fp16 ----
 // IEEE 754 binary16 <-> binary32, written from the format definition:
@@ -228,6 +230,37 @@ void decode_q4_k(const uint8_t* blk, uint8_t q[kQK], uint8_t sc[8], uint8_t m[8]
 int64_t planar_bytes(int64_t rows, int K) {
   const int64_t groups = (rows + kTileRows - 1) / kTileRows;
   return groups * (int64_t)(K / kQK) * kTileBytes;
+}
+
+// Planar Q4_K tile T(g, b), 2304 bytes, lane L = 16u + i (u = half of the
+// block: sub-blocks 4u..4u+3):
+//   [512j + 16L, +16),  j=0..3 : qs[64u + 16j .. +15]
+//   [2048 + 16i, +16)           : the 16-byte header (d, dmin, scales[12])
+int64_t planar_bytes_q4(int64_t rows, int K) {
+  const int64_t groups = (rows + kTileRows - 1) / kTileRows;
+  return groups * (int64_t)(K / kQK) * kTileBytesQ4;
+}
+
+void block_to_tile_q4(const uint8_t* blk, int i, uint8_t* tile) {
+  for (int u = 0; u < 2; ++u)
+    for (int j = 0; j < 4; ++j)
+      std::memcpy(tile + 512 * j + 16 * (16 * u + i), blk + 16 + 64 * u + 16 * j, 16);
+  std::memcpy(tile + 2048 + 16 * i, blk, 16);
+}
+
+void tile_to_block_q4(const uint8_t* tile, int i, uint8_t* blk) {
+  for (int u = 0; u < 2; ++u)
+    for (int j = 0; j < 4; ++j)
+      std::memcpy(blk + 16 + 64 * u + 16 * j, tile + 512 * j + 16 * (16 * u + i), 16);
+  std::memcpy(blk, tile + 2048 + 16 * i, 16);
+}
+
+void unpack_planar_q4(const uint8_t* P, int64_t rows, int K, uint8_t* W) {
+  const int nb = K / kQK;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int b = 0; b < nb; ++b)
+      tile_to_block_q4(P + ((r / kTileRows) * nb + b) * kTileBytesQ4, (int)(r % kTileRows),
+                       W + (r * nb + b) * kQ4KBytes);
 }
 
 // Copies one GGUF block (row i of tile) into / out of its tile slots.
@@ -397,6 +430,24 @@ void orc_decode_q4_k(const uint8_t* blk, uint8_t* q256, uint8_t* sc8, uint8_t* m
 }
 
 int64_t orc_planar_bytes(int64_t rows, int K) { return planar_bytes(rows, K); }
+int64_t orc_planar_bytes_q4(int64_t rows, int K) { return planar_bytes_q4(rows, K); }
+
+int orc_repack_planar_q4(const uint8_t* W, int64_t rows, int K, uint8_t* P) {
+  if (rows <= 0 || K <= 0 || K % kQK != 0) return -2;
+  const int nb = K / kQK;
+  std::memset(P, 0, (size_t)planar_bytes_q4(rows, K));
+  for (int64_t r = 0; r < rows; ++r)
+    for (int b = 0; b < nb; ++b)
+      block_to_tile_q4(W + (r * nb + b) * kQ4KBytes, (int)(r % kTileRows),
+                       P + ((r / kTileRows) * nb + b) * kTileBytesQ4);
+  return 0;
+}
+
+int orc_unpack_planar_q4(const uint8_t* P, int64_t rows, int K, uint8_t* W) {
+  if (rows <= 0 || K <= 0 || K % kQK != 0) return -2;
+  unpack_planar_q4(P, rows, K, W);
+  return 0;
+}
 
 int orc_repack_planar(const uint8_t* W, int64_t rows, int K, uint8_t* P) {
   if (rows <= 0 || K <= 0 || K % kQK != 0) return -2;
@@ -449,6 +500,12 @@ int orc_gemv(int type, const uint8_t* W, int64_t rows, int K, const uint8_t* xq,
     gemv_gguf(kTypeQ6K, g.data(), rows, K, xq, ncols, nullptr, y, rows, bound, nullptr);
     return 0;
   }
+  if (type == kTypeQ4KPlanar) {
+    std::vector<uint8_t> g((size_t)(rows * (K / kQK) * kQ4KBytes));
+    unpack_planar_q4(W, rows, K, g.data());
+    gemv_gguf(kTypeQ4K, g.data(), rows, K, xq, ncols, nullptr, y, rows, bound, nullptr);
+    return 0;
+  }
   return -1;
 }
 
@@ -465,6 +522,12 @@ int orc_block_sums(int type, const uint8_t* W, int64_t rows, int K, const uint8_
     std::vector<uint8_t> g((size_t)(rows * (K / kQK) * kQ6KBytes));
     unpack_planar(W, rows, K, g.data());
     gemv_gguf(kTypeQ6K, g.data(), rows, K, xq, ncols, nullptr, y.data(), rows, nullptr, sumi);
+    return 0;
+  }
+  if (type == kTypeQ4KPlanar) {
+    std::vector<uint8_t> g((size_t)(rows * (K / kQK) * kQ4KBytes));
+    unpack_planar_q4(W, rows, K, g.data());
+    gemv_gguf(kTypeQ4K, g.data(), rows, K, xq, ncols, nullptr, y.data(), rows, nullptr, sumi);
     return 0;
   }
   return -1;

@@ -45,8 +45,10 @@ def test_version_and_strerror(lib):
 def test_planar_bytes_host_only(lib):
     assert mmvq.planar_bytes(151936, 2560) == 151936 // 16 * 10 * 3360 == 151936 * 10 * 210
     assert mmvq.planar_bytes(17, 256) == 2 * 1 * 3360
-    assert lib.mmvq_planar_bytes(16, 100) == -1
-    assert lib.mmvq_planar_bytes(0, 256) == -1
+    assert mmvq.planar_bytes(17, 512, mmvq.TYPE_Q4_K) == 2 * 2 * 2304
+    assert lib.mmvq_planar_bytes(14, 16, 100) == -1
+    assert lib.mmvq_planar_bytes(14, 0, 256) == -1
+    assert lib.mmvq_planar_bytes(1014, 16, 256) == -1
 
 
 A = 0x10000  # an aligned fake device address: never dereferenced, calls fail before CUDA
@@ -66,6 +68,8 @@ A = 0x10000  # an aligned fake device address: never dereferenced, calls fail be
     ((14, A + 8, 16, 256, A, 1, A, None), mmvq.ERR_ALIGN),
     ((1014, A, 16, 256, A + 4, 1, A, None), mmvq.ERR_ALIGN),
     ((12, A, 16, 256, A, 1, A + 2, None), mmvq.ERR_ALIGN),
+    ((1012, A + 4, 16, 256, A, 1, A, None), mmvq.ERR_ALIGN),
+    ((1012, A, 16, 200, A, 1, A, None), mmvq.ERR_SHAPE),
 ])
 def test_gemv_rejects_bad_arguments_on_host(lib, args, code):
     assert lib.mmvq_gemv(*args) == code
@@ -79,6 +83,7 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_quantize_q8_1(A, 64, 1, 64, A + 4, None) == mmvq.ERR_ALIGN
     assert L.mmvq_quantize_q8_1(A, 64, 0, 64, A, None) == mmvq.ERR_SHAPE
     g = (12, A, 256, 1536, 2560, A, A, 256, A, A, 1, A, None, None)
+    assert L.mmvq_grouped(1012, A, 256, 1530, 2560, A, A, 256, A, A, 1, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_grouped(*g[:0], 14 + 1000, *g[1:]) == mmvq.ERR_TYPE
     assert L.mmvq_grouped(*g[:7], 0, *g[8:]) == mmvq.ERR_ROUTING
     assert L.mmvq_grouped(*g[:7], 4097, *g[8:]) == mmvq.ERR_ROUTING
@@ -90,7 +95,8 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_route_groups(None, 4, 8, 256, A, A, A, A, None, None) == mmvq.ERR_NULL
     assert L.mmvq_silu_mul_quantize_q8_1(A, 768 + 16, 1, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_silu_mul_quantize_q8_1(A, 768, 0, A, None, None) == mmvq.ERR_SHAPE
-    assert L.mmvq_repack_planar(12, A, 16, 256, A, None) == mmvq.ERR_TYPE
+    assert L.mmvq_repack_planar(99, A, 16, 256, A, None) == mmvq.ERR_TYPE
+    assert L.mmvq_repack_planar(12, A + 8, 16, 256, A, None) == mmvq.ERR_ALIGN
     assert L.mmvq_repack_planar(14, A, 16, 256, A + 8, None) == mmvq.ERR_ALIGN
     assert L.mmvq_gather_planar_rows(A, 16, 256, A, 0, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_gather_planar_rows(A, 16, 256, A, 4, A + 8, None, None) == mmvq.ERR_ALIGN

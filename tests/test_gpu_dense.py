@@ -19,6 +19,7 @@ KINDS = {
     "q6_k": (mmvq.TYPE_Q6_K, oracle.TYPE_Q6_K, synth.q6_k_weights),
     "q6_k_planar": (mmvq.TYPE_Q6_K_PLANAR, oracle.TYPE_Q6_K, synth.q6_k_weights),
     "q4_k": (mmvq.TYPE_Q4_K, oracle.TYPE_Q4_K, synth.q4_k_weights),
+    "q4_k_planar": (mmvq.TYPE_Q4_K_PLANAR, oracle.TYPE_Q4_K, synth.q4_k_weights),
 }
 
 
@@ -28,6 +29,8 @@ def _weights(kind, rows, K, salt):
     Wd = dev(W)
     if kind == "q6_k_planar":
         Wd = mmvq.repack_planar(Wd, rows, K)
+    if kind == "q4_k_planar":
+        Wd = mmvq.repack_planar(Wd, rows, K, type_=mmvq.TYPE_Q4_K)
     return W, Wd, t_gpu, t_orc
 
 

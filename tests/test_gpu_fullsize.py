@@ -50,12 +50,17 @@ def test_q6_k_sweep_shapes(rows, K, planar):
 
 @pytest.mark.parametrize("rows,K", [(12288, 2560), (6144, 2560), (2560, 6144), (640, 2560),
                                     (512, 2560)])
-def test_q4_k_dense_shapes(rows, K):
+@pytest.mark.parametrize("planar", [True, False])
+def test_q4_k_dense_shapes(rows, K, planar):
     W = synth.q4_k_weights(rows, K, salt=rows + K)
     Wd = dev(W)
+    t = mmvq.TYPE_Q4_K
+    if planar:
+        Wd = mmvq.repack_planar(Wd, rows, K, type_=mmvq.TYPE_Q4_K)
+        t = mmvq.TYPE_Q4_K_PLANAR
     for ncols in (1, 4):
         x = synth.activations(K, ncols, salt=ncols)
-        _check_sampled(mmvq.TYPE_Q4_K, oracle.TYPE_Q4_K, W, Wd, rows, K, x, ncols, salt=ncols)
+        _check_sampled(t, oracle.TYPE_Q4_K, W, Wd, rows, K, x, ncols, salt=ncols)
 
 
 def test_lm_head_and_draft_head():

@@ -23,6 +23,13 @@ def test_repack_bit_exact(rows, K):
                           oracle.repack_planar(W, rows, K))
 
 
+@pytest.mark.parametrize("rows,K", [(1, 256), (16, 256), (37, 512), (300, 2560), (45, 10240)])
+def test_repack_q4_bit_exact(rows, K):
+    W = synth.q4_k_weights(rows, K, salt=rows)
+    got = host(mmvq.repack_planar(dev(W), rows, K, type_=mmvq.TYPE_Q4_K))
+    assert np.array_equal(got, oracle.repack_planar(W, rows, K, oracle.TYPE_Q4_K))
+
+
 @pytest.mark.parametrize("rows,K,n", [(300, 512, 37), (1000, 2560, 64), (40, 256, 1)])
 def test_gather_bit_exact(rows, K, n):
     W = synth.q6_k_weights(rows, K, salt=n)
@@ -60,14 +67,17 @@ def test_route_groups_bit_exact(T, k, E):
 
 
 def _grouped_case(kind, T, k, E, rows, K, salt):
-    t = {"q4_k": (mmvq.TYPE_Q4_K, oracle.TYPE_Q4_K), "q6_k": (mmvq.TYPE_Q6_K, oracle.TYPE_Q6_K)}[kind]
-    W = synth.expert_weights(kind, E, rows, K, salt=salt)
+    t = {"q4_k": (mmvq.TYPE_Q4_K, oracle.TYPE_Q4_K), "q6_k": (mmvq.TYPE_Q6_K, oracle.TYPE_Q6_K),
+         "q4_k_planar": (mmvq.TYPE_Q4_K_PLANAR, oracle.TYPE_Q4_K)}[kind]
+    W = synth.expert_weights(kind.replace("_planar", ""), E, rows, K, salt=salt)
     topk = synth.routing(T, k, E, salt=salt)
     eids, offs, act, _ = oracle.route_groups(topk, E)
     x = synth.activations(K, T, salt=salt)
     xq = oracle.quantize_q8_1(x)
     y_ref, bound = oracle.grouped(t[1], W, E, rows, K, eids, offs, act, xq, with_bound=True)
     Wd = dev(W)
+    if kind == "q4_k_planar":
+        Wd = torch.cat([mmvq.repack_planar(dev(W[e]), rows, K, type_=mmvq.TYPE_Q4_K) for e in range(E)])
     xqd = mmvq.quantize_q8_1(dev(x))
     g_eids, g_offs, g_act, _, _ = mmvq.route_groups(dev(topk), E)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -75,16 +85,18 @@ def _grouped_case(kind, T, k, E, rows, K, salt):
     return host(y), y_ref, bound, host(status)[0]
 
 
+@pytest.mark.parametrize("kind", ["q4_k", "q4_k_planar"])
 @pytest.mark.parametrize("T", [1, 4, 8])
-def test_grouped_gate_up_shape(T):
+def test_grouped_gate_up_shape(kind, T):
     # 256 experts, gate|up 1536 x 2560, top-8 distinct experts per token
-    y, y_ref, bound, st = _grouped_case("q4_k", T, 8, 256, 1536, 2560, salt=T)
+    y, y_ref, bound, st = _grouped_case(kind, T, 8, 256, 1536, 2560, salt=T)
     assert st == 0
     assert_within_bound(y, y_ref, bound, f"GU T={T}")
 
 
+@pytest.mark.parametrize("planar", [False, True])
 @pytest.mark.parametrize("T", [1, 8])
-def test_grouped_down_shape(T):
+def test_grouped_down_shape(T, planar):
     # down 2560 x 768, activations are the requantised SiLU*up columns, one per position
     E, rows, K, k = 256, 2560, 768, 8
     W = synth.expert_weights("q4_k", E, rows, K, salt=10 + T)
@@ -95,15 +107,18 @@ def test_grouped_down_shape(T):
     y_ref, bound = oracle.grouped(oracle.TYPE_Q4_K, W, E, rows, K, eids, offs, None, xq,
                                   with_bound=True)
     g_eids, g_offs, _, _, _ = mmvq.route_groups(dev(topk), E)
-    y = mmvq.grouped(mmvq.TYPE_Q4_K, dev(W), E, rows, K, g_eids, g_offs, None,
-                     mmvq.quantize_q8_1(dev(h)), T * k, T * k)
+    Wd, t = dev(W), mmvq.TYPE_Q4_K
+    if planar:
+        Wd = torch.cat([mmvq.repack_planar(dev(W[e]), rows, K, type_=mmvq.TYPE_Q4_K) for e in range(E)])
+        t = mmvq.TYPE_Q4_K_PLANAR
+    y = mmvq.grouped(t, Wd, E, rows, K, g_eids, g_offs, None, mmvq.quantize_q8_1(dev(h)), T * k, T * k)
     assert_within_bound(host(y), y_ref, bound, f"down T={T}")
 
 
-@pytest.mark.parametrize("kind", ["q4_k", "q6_k"])
-def test_grouped_groups_larger_than_eight_and_ragged_rows(kind):
+@pytest.mark.parametrize("kind,rows", [("q4_k", 37), ("q6_k", 37), ("q4_k_planar", 48)])
+def test_grouped_groups_larger_than_eight_and_ragged_rows(kind, rows):
     # 4 experts, 20 tokens, top-2: groups of about 10 positions (processed 8 at a time)
-    y, y_ref, bound, st = _grouped_case(kind, 20, 2, 4, 37, 512, salt=3)
+    y, y_ref, bound, st = _grouped_case(kind, 20, 2, 4, rows, 512, salt=3)
     assert st == 0
     assert_within_bound(y, y_ref, bound, kind)
 

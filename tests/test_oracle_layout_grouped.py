@@ -79,6 +79,38 @@ def test_planar_product_equals_gguf_product():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("rows,K", [(16, 256), (37, 512), (5, 2560)])
+def test_planar_q4_round_trip_size_and_product(rows, K):
+    W = synth.q4_k_weights(rows, K, salt=rows)
+    P = oracle.repack_planar(W, rows, K, oracle.TYPE_Q4_K)
+    assert P.size == -(-rows // 16) * (K // 256) * 2304 == oracle.planar_bytes(rows, K, oracle.TYPE_Q4_K)
+    assert np.array_equal(oracle.unpack_planar(P, rows, K, oracle.TYPE_Q4_K), W)
+    xq = oracle.quantize_q8_1(synth.activations(K, 2, salt=rows))
+    assert np.array_equal(oracle.gemv(oracle.TYPE_Q4_K, W, rows, K, xq, 2),
+                          oracle.gemv(oracle.TYPE_Q4_K_PLANAR, P, rows, K, xq, 2))
+
+
+def test_planar_q4_marker_bytes_land_per_spec():
+    rows, K = 40, 512
+    nb = K // 256
+    W = np.zeros((rows, nb, 144), np.uint8)
+    cases = [(0, 0, 0), (1, 1, 15), (17, 0, 16), (39, 1, 79), (5, 1, 80), (22, 0, 143), (31, 1, 3)]
+    for k, (r, b, off) in enumerate(cases):
+        W[r, b, off] = 1 + k
+    P = oracle.repack_planar(W, rows, K, oracle.TYPE_Q4_K)
+    for k, (r, b, off) in enumerate(cases):
+        g, i = divmod(r, 16)
+        base = (g * nb + b) * 2304
+        if off < 16:                                   # header
+            pos = base + 2048 + 16 * i + off
+        else:                                          # qs[64u + 16j + e]
+            u, rem = divmod(off - 16, 64)
+            j, e = divmod(rem, 16)
+            pos = base + 512 * j + 16 * (16 * u + i) + e
+        assert P[pos] == 1 + k, (r, b, off)
+    assert np.count_nonzero(P) == len(cases)
+
+
 def test_gather_planar_rows_picks_the_named_rows():
     rows, K = 300, 512
     W = synth.q6_k_weights(rows, K, salt=4)
