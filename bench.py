@@ -79,6 +79,35 @@ WORKLOAD_DESC = {
 }
 
 
+def kernel_source_hash() -> str:
+    """sha256 of the CUDA sources and the ABI header (the kernels as built)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(HERE, "block_quantized_matvec_gb300", "csrc", "*"))) + \
+            [os.path.join(HERE, "include", "mmvq.h")]:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(summary: str):
+    """DRAM bytes per MMVQ launch from a committed ncu summary, or None when
+    the summary is missing or was taken on different kernel sources."""
+    try:
+        text = open(os.path.join(HERE, "profiles", summary)).read()
+    except OSError:
+        return None
+    fields = dict(l.split(": ", 1) for l in text.splitlines() if ": " in l and not l.startswith("|"))
+    if fields.get("kernel_source_sha256", "").strip() != kernel_source_hash():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_mmvq_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def load_peak():
     p = os.path.join(HERE, "MEASURED_PEAKS.json")
     try:
@@ -359,9 +388,12 @@ def run_ours(args, rank, world, local_rank):
                    "step": "per case: Q8_1-quantise its columns once, then one MMVQ per weight copy",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 3), "traffic": None,
+                     "frac": round(achieved / peak, 3),
+                     "traffic": (profiled_traffic("mmvq_q6k_sweep_launch_list.md")
+                                 if args.workload == "q6k_sweep" else None),
+                     "algorithmic_bytes_per_launch": round(alg_step / len(calls)),
                      "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": "mmvq_dense_kernel (all MMVQ launches of the last timed step)"},
+                     "kernel": "MMVQ kernel, all launches of the last timed step"},
         "e2e": {"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
                 "steps": e2e_steps},
