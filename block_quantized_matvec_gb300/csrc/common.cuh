@@ -102,11 +102,9 @@ __device__ __forceinline__ void stage_q8_1(const uint8_t* __restrict__ xq, int K
                                            int tid, int nthreads) {
   const int nbq = K / kQK8;
   const int vec_per_col = nbq * 9 / 4;  // 16-byte vectors per column
-  const int total = ncols * vec_per_col;
   const int rb = act_row_bytes(K);
-  for (int v = tid; v < total; v += nthreads) {
-    const int c = v / vec_per_col;
-    const int vi = v - c * vec_per_col;
+  for (int c = 0; c < ncols; ++c)
+  for (int vi = tid; vi < vec_per_col; vi += nthreads) {
     const int col = col_of(c);
     uint4 q = make_uint4(0u, 0u, 0u, 0u);
     if (col >= 0)

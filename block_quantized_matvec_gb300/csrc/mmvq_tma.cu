@@ -60,10 +60,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(20000)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -73,13 +73,23 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 // Waits for the phase with the given parity to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// The timer is read once every 64 tries; `backoff_ns` > 0 sleeps between
+// tries (the producer, whose waits are not on the critical path).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int backoff_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (backoff_ns) __nanosleep(backoff_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      const uint64_t t = global_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kWaitLimitNs) {
+        return false;
+      }
+    }
   }
-  return true;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -183,24 +193,33 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
 
   if (warp == C) {  // ------------------------------------------ producer
     if (lane == 0) {
+      // slot and round parity are kept incrementally (no divisions per stage)
       int64_t it = 0;
+      int slot = 0;
+      uint32_t par = 0;
+      int64_t j = 0;
+      int bb = 0;
       for (; it < total; ++it) {
-        const int s = (int)(it % S);
-        const int64_t round = it / S;
-        if (round > 0 && !*fail && !mbar_wait(&empty[s], (uint32_t)((round - 1) & 1))) {
+        if (it >= S && !*fail && !mbar_wait(&empty[slot], par ^ 1u, 128)) {
           *fail = 1;
           atomicOr(&g_fault_word, kFaultMbarTimeout);
         }
         if (*fail) break;
-        const int64_t j = it / spb;
-        const int bb = (int)(it % spb);
         const int64_t left = my_rgs - j * G;
         const int valid = (int)(left < G ? left : G);
-        mbar_expect_tx(&full[s], (uint32_t)(valid * P * TB));
+        mbar_expect_tx(&full[slot], (uint32_t)(valid * P * TB));
         for (int g = 0; g < valid; ++g) {
           const int64_t rg = blockIdx.x + (j * G + g) * (int64_t)gridDim.x;
-          bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)g * P * TB,
-                   W + (rg * nb + (int64_t)bb * P) * TB, (uint32_t)(P * TB), &full[s]);
+          bulk_g2s(ring + (size_t)slot * stage_bytes + (size_t)g * P * TB,
+                   W + (rg * nb + (int64_t)bb * P) * TB, (uint32_t)(P * TB), &full[slot]);
+        }
+        if (++bb == spb) {
+          bb = 0;
+          ++j;
+        }
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1u;
         }
       }
       // no copy of this CTA may land after it exits: wait (bounded) for the
@@ -231,6 +250,8 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   const int p = warp - g * P;
   const int i = lane & 15;
   const int h = lane >> 4;
+  int slot = 0;
+  uint32_t par = 0;
   for (int64_t j = 0; j < batches; ++j) {
     const int64_t k = j * G + g;
     const bool valid = k < my_rgs;
@@ -245,11 +266,14 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
 #pragma unroll
     for (int c = 0; c < NCOLS; ++c) acc[c] = 0.0f;
     for (int bb = 0; bb < spb; ++bb) {
-      const int64_t it = j * spb + bb;
-      const int s = (int)(it % S);
-      if (!*fail && !mbar_wait(&full[s], (uint32_t)((it / S) & 1))) {
+      const int s = slot;
+      if (!*fail && !mbar_wait(&full[s], par)) {
         *fail = 1;
         atomicOr(&g_fault_word, kFaultMbarTimeout);
+      }
+      if (++slot == S) {
+        slot = 0;
+        par ^= 1u;
       }
       const uint8_t* tile = ring + (size_t)s * stage_bytes + (size_t)warp * TB;
       if (LAYOUT == kQ4Planar) {
