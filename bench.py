@@ -470,19 +470,23 @@ def run_moe(args, rank, world, local_rank):
     for r in range(R):
         step(r)
     torch.cuda.synchronize()
-    graphs, events = [], []
+    # timed graphs: the five kernels back to back (each may start while its
+    # predecessor drains); breakdown graphs: the same with an event node
+    # between kernels, replayed after the timed region
+    graphs, graphs_ev, events = [], [], []
     for r in range(R):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         for e in evs:
             e.record()
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(device=dev)
-        cap.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
-            step(r, torch.cuda.current_stream(), evs)
-        torch.cuda.synchronize()
-        graphs.append(g)
+        for with_ev in (False, True):
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(device=dev)
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                step(r, torch.cuda.current_stream(), evs if with_ev else None)
+            torch.cuda.synchronize()
+            (graphs_ev if with_ev else graphs).append(g)
         events.append(evs)
 
     stream = torch.cuda.current_stream()
@@ -503,12 +507,19 @@ def run_moe(args, rank, world, local_rank):
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
 
+    dur_runs = []
+    for rep in range(4):
+        for r in range(R):
+            graphs_ev[r].replay()
+            torch.cuda.synchronize()
+            evs = events[r]
+            dur_runs.append([evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(5)])
+
     distinct = [len(np.unique(t)) for t in topks]
     step_bytes = [metrics.moe_step_bytes(d, H, F) for d in distinct]
     total_bytes = sum(step_bytes[i % R] for i in range(args.steps))
     names = ["quantize", "route", "grouped_gate_up", "silu_requant", "grouped_down"]
-    dur = np.array([[evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(5)] for evs in events])
-    mean_us = dur.mean(axis=0)
+    mean_us = np.array(dur_runs).mean(axis=0)
     gu_bytes = np.mean([d * metrics.weight_bytes("q4_k", 2 * F, H) for d in distinct])
     dn_bytes = np.mean([d * metrics.weight_bytes("q4_k", H, F) for d in distinct])
     peak, peak_kind = load_peak()
@@ -532,7 +543,8 @@ def run_moe(args, rank, world, local_rank):
         "data": "synthetic (seeded generators shaped like the pages' matrices)",
         "config": {"workload": WORKLOAD_DESC[args.workload], "tokens": T, "routings": R,
                    "distinct_experts_mean": float(np.mean(distinct)),
-                   "timing": "CUDA graph replay; event nodes between the five kernels"},
+                   "timing": "CUDA graph replay of whole steps; per-kernel times from a "
+                             "second graph with event nodes between the five kernels"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": None,
                      "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "grouped gate|up MMVQ"},

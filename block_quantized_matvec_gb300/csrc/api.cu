@@ -106,11 +106,12 @@ int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, i
                  const int32_t* expert_ids, const int32_t* token_offsets, int n_groups,
                  const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
                  int32_t* status, mmvq_stream_t stream) {
-  if (type != MMVQ_Q4_K && type != MMVQ_Q6_K && type != MMVQ_Q4_K_PLANAR) return MMVQ_ERR_TYPE;
+  if (!dense_type(type)) return MMVQ_ERR_TYPE;
   if (!W_experts || !expert_ids || !token_offsets || !xq || !y) return MMVQ_ERR_NULL;
   int rc = check_weights_shape(rows, K);
   if (rc) return rc;
-  if (type == MMVQ_Q4_K_PLANAR && rows % mmvq::kTileRows != 0) return MMVQ_ERR_SHAPE;
+  if ((type == MMVQ_Q4_K_PLANAR || type == MMVQ_Q6_K_PLANAR) && rows % mmvq::kTileRows != 0)
+    return MMVQ_ERR_SHAPE;
   if (n_experts < 1 || n_xq_cols < 1) return MMVQ_ERR_SHAPE;
   if (n_groups < 1 || n_groups > 4096) return MMVQ_ERR_ROUTING;
   if (!aligned(W_experts, 16) || !aligned(xq, 16) || !aligned(y, 4) || !aligned(expert_ids, 4) ||

@@ -165,7 +165,7 @@ template <int LAYOUT, int NCOLS>
 static int dense_config(int64_t rows, int K, DenseCfg* out) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, DenseCfg> cache;
-  static size_t smem_set = 48 * 1024;
+  static size_t smem_set = 0;  // the attribute is set before the first launch
   const uint64_t key = ((uint64_t)rows << 8) | (uint64_t)(K / kQK);
   {
     std::lock_guard<std::mutex> lock(mu);

@@ -187,7 +187,7 @@ static int launch_grouped_t(const uint8_t* W, int n_experts, int64_t rows, int K
   }
   if (smem > limit) return MMVQ_ERR_SHAPE;
   static std::mutex mu;
-  static size_t smem_set = 48 * 1024;
+  static size_t smem_set = 0;  // the attribute is set before the first launch
   if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * wk, smem) != cudaSuccess ||
@@ -199,6 +199,11 @@ static int launch_grouped_t(const uint8_t* W, int n_experts, int64_t rows, int K
   return launch_pdl(kern, dim3(grid), dim3(32, wk, 1), smem, stream, W, n_experts, rows, K,
                     expert_ids, offsets, n_groups, act_index, xq, n_xq_cols, y, status);
 }
+
+int launch_grouped_tma(int type, const void* W, int n_experts, int64_t rows, int K,
+                       const int32_t* expert_ids, const int32_t* offsets, int n_groups,
+                       const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
+                       int32_t* status, cudaStream_t s);
 
 int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,
                    const int32_t* expert_ids, const int32_t* offsets, int n_groups,
@@ -214,8 +219,9 @@ int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,
       return launch_grouped_t<kQ6Gguf>(w, n_experts, rows, K, expert_ids, offsets, n_groups,
                                        act_index, x, n_xq_cols, y, status, s);
     case MMVQ_Q4_K_PLANAR:
-      return launch_grouped_t<kQ4Planar>(w, n_experts, rows, K, expert_ids, offsets, n_groups,
-                                         act_index, x, n_xq_cols, y, status, s);
+    case MMVQ_Q6_K_PLANAR:
+      return launch_grouped_tma(type, W, n_experts, rows, K, expert_ids, offsets, n_groups,
+                                act_index, xq, n_xq_cols, y, status, s);
   }
   return MMVQ_ERR_TYPE;
 }

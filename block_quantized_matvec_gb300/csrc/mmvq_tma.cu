@@ -321,6 +321,321 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   }
 }
 
+// ------------------------------------------------- grouped (experts) ----
+// Grouped expert MMVQ on the same ring ("Strata" PR #2746 "B70 validation":
+// grouped calls over per-expert token groups, empty groups allowed; issue
+// #2801: the grouped gate/up and down kernels).  Each CTA compacts the
+// non-empty groups from the offsets (after the grid dependency: the lists
+// come from the preceding kernel) and takes an equal contiguous range of
+// items; an item is G consecutive row groups of one group's expert.  Per
+// item and per chunk of up to CM positions a stage holds, for each of the G
+// row groups, P consecutive tiles (one bulk copy each); consumer warp (g, p)
+// takes row group g and the K-slice p.  Producer and consumers walk the same
+// (item, chunk, stage) sequence, so their slot and phase counters agree.
+
+constexpr int kMaxGroupsTma = 4096;
+
+__device__ __forceinline__ int block_scan_excl(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int t = warp_sums[w];
+      warp_sums[w] = run;
+      run += t;
+    }
+    warp_sums[nwarps] = run;
+  }
+  __syncthreads();
+  const int out = warp_sums[warp] + x - v;
+  *total = warp_sums[nwarps];
+  __syncthreads();
+  return out;
+}
+
+struct GroupedRing {
+  const uint8_t* ring;
+  size_t stage_bytes;
+  uint64_t* full;
+  uint64_t* empty;
+  volatile int* fail;
+  int S;
+};
+
+// One (item, chunk) for consumer warp (g, p): row group rg, K-slice p.
+template <int LAYOUT, int NC>
+__device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot, uint32_t& par,
+                                                int g, int p, int P, int lane, int spb,
+                                                const uint8_t* act, int rb, const float* da,
+                                                const float* sa, int nbq, float* red,
+                                                float* ybase, int64_t rg, bool valid,
+                                                int64_t rows) {
+  constexpr int TB = tile_bytes(LAYOUT);
+  const int i = lane & 15;
+  const int h = lane >> 4;
+  float acc[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
+  const size_t tile_off = (size_t)(g * P + p) * TB;
+  for (int bb = 0; bb < spb; ++bb) {
+    const int s = slot;
+    if (!*r.fail && !mbar_wait(&r.full[s], par)) {
+      *r.fail = 1;
+      atomicOr(&g_fault_word, kFaultMbarTimeout);
+    }
+    if (++slot == r.S) {
+      slot = 0;
+      par ^= 1u;
+    }
+    // a row group past the end reads a stale (in-bounds) tile and stores nothing
+    const uint8_t* tile = r.ring + (size_t)s * r.stage_bytes + tile_off;
+    if (LAYOUT == kQ4Planar) {
+      Q4Half w;
+      load_q4_tile_smem(tile, lane, w);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&r.empty[s]);
+      if (valid) q4_dot<NC>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, nullptr, 0);
+    } else {
+      Q6Half w;
+      load_q6_tile_smem(tile, lane, w);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&r.empty[s]);
+      if (valid) q6_dot<NC>(w, h, bb * P + p, act, rb, da, nbq, acc, nullptr, 0);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
+  const int64_t row = rg * kTileRows + i;
+  if (P == 1) {
+    if (valid && h == 0 && row < rows) {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) ybase[c * rows + row] = acc[c];
+    }
+    return;
+  }
+  float* rg_red = red + (size_t)g * P * kMaxCols * kTileRows;
+  if (h == 0) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) rg_red[(p * kMaxCols + c) * kTileRows + i] = acc[c];
+  }
+  group_sync(2 + g, 32 * P);
+  if (p == 0 && valid && h == 0 && row < rows) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float sum = 0.0f;
+      for (int q = 0; q < P; ++q) sum += rg_red[(q * kMaxCols + c) * kTileRows + i];
+      ybase[c * rows + row] = sum;
+    }
+  }
+  group_sync(2 + g, 32 * P);
+}
+
+__host__ __device__ inline size_t grouped_smem_bytes(int layout, int S, int K, int CM, int G,
+                                                     int P) {
+  return tma_ring_offset(S) + (size_t)S * G * P * tile_bytes(layout) +
+         (size_t)CM * act_row_bytes(K) + (size_t)CM * (K / kQK8) * 8 +
+         (size_t)G * P * kMaxCols * kTileRows * 4;
+}
+
+template <int LAYOUT, int CM>
+__global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
+    const uint8_t* __restrict__ W, int n_experts, int64_t rows, int K,
+    const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ offsets, int n_groups,
+    const int32_t* __restrict__ act_index, const uint8_t* __restrict__ xq, int n_xq_cols,
+    float* __restrict__ y, int32_t* __restrict__ status, int S, int G, int P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int active[kMaxGroupsTma];
+  __shared__ int warp_sums[17];
+  __shared__ int cols_s[kMaxCols];
+  constexpr int TB = tile_bytes(LAYOUT);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int C = G * P;
+  const int nb = K / kQK;
+  const int nbq = K / kQK8;
+  const int rb = act_row_bytes(K);
+  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
+  const int64_t n_rgb = (n_rg + G - 1) / G;
+  const int spb = nb / P;
+  const size_t slice_bytes = (size_t)P * TB;
+  const int64_t expert_bytes = n_rg * nb * TB;
+
+  GroupedRing r;
+  r.full = reinterpret_cast<uint64_t*>(smem);
+  r.empty = r.full + S;
+  r.fail = reinterpret_cast<volatile int*>(r.empty + S);
+  r.ring = smem + tma_ring_offset(S);
+  r.stage_bytes = (size_t)G * slice_bytes;
+  r.S = S;
+  uint8_t* ring = smem + tma_ring_offset(S);
+  uint8_t* act = ring + (size_t)S * r.stage_bytes;
+  float* da = reinterpret_cast<float*>(act + (size_t)CM * rb);
+  float* sa = da + CM * nbq;
+  float* red = sa + CM * nbq;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&r.full[s], 1);
+      mbar_init(&r.empty[s], C);
+    }
+    *r.fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  grid_launch_dependents();
+  grid_dependency_wait();
+
+  // 1. compact the valid non-empty groups, in group order (all threads)
+  const int per = (n_groups + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int g0 = threadIdx.x * per;
+  const int g1 = min(n_groups, g0 + per);
+  int cnt = 0;
+  bool bad = false;
+  for (int q = g0; q < g1; ++q) {
+    const int e = expert_ids[q];
+    const int o0 = offsets[q], o1 = offsets[q + 1];
+    const bool ok = e >= 0 && e < n_experts && o0 >= 0 && o1 >= o0;
+    bad |= !ok;
+    cnt += (ok && o1 > o0) ? 1 : 0;
+  }
+  if (bad && status && blockIdx.x == 0) *status = MMVQ_ERR_ROUTING;
+  int n_active = 0;
+  int pos = block_scan_excl(cnt, warp_sums, &n_active);
+  for (int q = g0; q < g1; ++q) {
+    const int e = expert_ids[q];
+    const int o0 = offsets[q], o1 = offsets[q + 1];
+    if (e >= 0 && e < n_experts && o0 >= 0 && o1 > o0) active[pos++] = q;
+  }
+  __syncthreads();
+
+  // 2. this CTA's contiguous share of the (group, row-group block) items
+  const int64_t n_items = (int64_t)n_active * n_rgb;
+  const int64_t it0 = n_items * blockIdx.x / gridDim.x;
+  const int64_t it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  if (it0 >= it1) return;
+  int a = (int)(it0 / n_rgb);
+  int64_t rgb = it0 - (int64_t)a * n_rgb;
+
+  if (warp == C) {  // ------------------------------------------ producer
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t par = 0;
+      int64_t issued = 0;
+      for (int64_t it = it0; it < it1 && !*r.fail; ++it) {
+        const int grp = active[a];
+        const uint8_t* Wexp = W + (size_t)expert_ids[grp] * expert_bytes;
+        const int64_t rg0 = rgb * G;
+        const int nvalid = (int)min((int64_t)G, n_rg - rg0);
+        const int pe = offsets[grp + 1];
+        for (int p0 = offsets[grp]; p0 < pe && !*r.fail; p0 += CM) {
+          for (int bb = 0; bb < spb; ++bb) {
+            if (issued >= S && !mbar_wait(&r.empty[slot], par ^ 1u, 128)) {
+              *r.fail = 1;
+              atomicOr(&g_fault_word, kFaultMbarTimeout);
+              break;
+            }
+            mbar_expect_tx(&r.full[slot], (uint32_t)(nvalid * slice_bytes));
+            uint8_t* dst = ring + (size_t)slot * r.stage_bytes;
+            const uint8_t* src = Wexp + (rg0 * nb + (int64_t)bb * P) * TB;
+            for (int g = 0; g < nvalid; ++g)
+              bulk_g2s(dst + (size_t)g * slice_bytes, src + (int64_t)g * nb * TB,
+                       (uint32_t)slice_bytes, &r.full[slot]);
+            ++issued;
+            if (++slot == S) {
+              slot = 0;
+              par ^= 1u;
+            }
+          }
+        }
+        if (++rgb == n_rgb) {
+          rgb = 0;
+          ++a;
+        }
+      }
+      // wait (bounded) for the last phase of every filled slot
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int64_t last = issued - 1 - ((issued - 1 - s) % S);
+        mbar_wait(&r.full[s], (uint32_t)((last / S) & 1));
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int nthreads = 32 * C;
+  const int g = warp / P;
+  const int p = warp - g * P;
+  int slot = 0;
+  uint32_t par = 0;
+  int staged_grp = -1, staged_p0 = -1;
+  for (int64_t it = it0; it < it1; ++it) {
+    const int grp = active[a];
+    const int pe = offsets[grp + 1];
+    const int64_t rg = rgb * G + g;
+    const bool valid = rg < n_rg;
+    for (int p0 = offsets[grp]; p0 < pe; p0 += CM) {
+      const int n = min(CM, pe - p0);
+      if (grp != staged_grp || p0 != staged_p0) {
+        group_sync(1, nthreads);  // the previous columns are no longer read
+        if (threadIdx.x < n) {
+          const int col = act_index ? act_index[p0 + threadIdx.x] : p0 + threadIdx.x;
+          const bool ok = col >= 0 && col < n_xq_cols;
+          if (!ok && status) *status = MMVQ_ERR_ROUTING;
+          cols_s[threadIdx.x] = ok ? col : -1;
+        }
+        group_sync(1, nthreads);
+        // an invalid column is staged as zeros: its outputs come out 0
+        stage_q8_1(xq, K, n, [&](int c) { return cols_s[c]; }, act, da,
+                   LAYOUT == kQ4Planar ? sa : nullptr, threadIdx.x, nthreads);
+        group_sync(1, nthreads);
+        staged_grp = grp;
+        staged_p0 = p0;
+      }
+      float* ybase = y + (size_t)p0 * rows;
+#define MMVQ_GC(NC)                                                                           \
+  grouped_consume<LAYOUT, NC>(r, slot, par, g, p, P, lane, spb, act, rb, da, sa, nbq, red, \
+                              ybase, rg, valid, rows)
+      if constexpr (CM == 1) {
+        MMVQ_GC(1);
+      } else if constexpr (CM == 2) {
+        if (n == 1) MMVQ_GC(1); else MMVQ_GC(2);
+      } else if constexpr (CM == 4) {
+        switch (n) {
+          case 1: MMVQ_GC(1); break;
+          case 2: MMVQ_GC(2); break;
+          case 3: MMVQ_GC(3); break;
+          default: MMVQ_GC(4); break;
+        }
+      } else {
+        switch (n) {
+          case 1: MMVQ_GC(1); break;
+          case 2: MMVQ_GC(2); break;
+          case 3: MMVQ_GC(3); break;
+          case 4: MMVQ_GC(4); break;
+          case 5: MMVQ_GC(5); break;
+          case 6: MMVQ_GC(6); break;
+          case 7: MMVQ_GC(7); break;
+          default: MMVQ_GC(8); break;
+        }
+      }
+#undef MMVQ_GC
+    }
+    if (++rgb == n_rgb) {
+      rgb = 0;
+      ++a;
+    }
+  }
+}
+
 // ------------------------------------------------------------ host side ----
 
 struct TmaCfg {
@@ -338,7 +653,7 @@ template <int LAYOUT, int NCOLS>
 static int tma_config(int64_t rows, int K, TmaCfg* out) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, TmaCfg> cache;
-  static size_t smem_set = 48 * 1024;
+  static size_t smem_set = 0;  // the attribute is set before the first launch
   const uint64_t key = ((uint64_t)rows << 8) | (uint64_t)(K / kQK);
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -488,6 +803,138 @@ static int tma_shape_layout(int64_t rows, int K, int ncols, int32_t* info) {
 int planar_tma_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
   if (type == MMVQ_Q4_K_PLANAR) return tma_shape_layout<kQ4Planar>(rows, K, ncols, info);
   return tma_shape_layout<kQ6Planar>(rows, K, ncols, info);
+}
+
+
+// ------------------------------------------------------ grouped launch ----
+
+struct GroupedCfg {
+  int G, P, S, per_sm;
+  size_t smem;
+};
+
+// Launch shape for the grouped ring kernel.  The number of non-empty groups
+// is only known on the device; `est_active` is an estimate from the call's
+// sizes, and R = est_active x row groups the work it implies.  Rules, from
+// sweeps of G, P and S on GB300 over the gate|up and down shapes of a
+// 256-expert MoE at 1-8 tokens:
+//  * P = 1 (whole rows per warp, no reduction) once R >= 8 x SMs, else the
+//    smallest divisor of K/256 above 1, so that enough warps are busy;
+//  * if some G <= 12 / P puts every item in one CTA per SM, the smallest
+//    such G with a ring as deep as fits (at most 6 stages): one wave, the
+//    most bytes in flight per SM;
+//  * otherwise G = 4 (at most 12 / P) and 3 stages, so that several CTAs
+//    share each SM.
+template <int LAYOUT, int CM>
+static int grouped_config(int64_t rows, int K, int64_t est_active, GroupedCfg* out) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, GroupedCfg> cache;
+  static size_t smem_set = 0;  // the attribute is set before the first launch
+  const uint64_t key = ((uint64_t)rows << 28) | ((uint64_t)(K / kQK) << 16) | (uint64_t)est_active;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return MMVQ_OK;
+    }
+  }
+  auto kern = mmvq_grouped_tma_kernel<LAYOUT, CM>;
+  const int sms = device_sms();
+  const size_t static_smem = (size_t)(kMaxGroupsTma + 17 + kMaxCols) * sizeof(int);
+  const size_t optin = max_smem_optin();
+  if (sms <= 0 || optin <= static_smem) return MMVQ_ERR_CUDA;
+  const size_t limit = optin - static_smem;
+  const int nb = K / kQK;
+  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
+  const int64_t R = est_active * n_rg;
+  int P = 1;
+  if (R < (int64_t)8 * sms)
+    for (int d = 2; d <= std::min(nb, 12); ++d)
+      if (nb % d == 0) {
+        P = d;
+        break;
+      }
+  int G = 0, S = 3;
+  for (int g = 1; g * P <= 12; ++g)
+    if (est_active * ((n_rg + g - 1) / g) <= sms) {
+      G = g;
+      S = 6;
+      break;
+    }
+  if (G == 0) G = std::max(1, std::min(4, 12 / P));
+  while (S > 2 && grouped_smem_bytes(LAYOUT, S, K, CM, G, P) > limit) --S;
+  const size_t smem = grouped_smem_bytes(LAYOUT, S, K, CM, G, P);
+  if (smem > limit) return MMVQ_ERR_SHAPE;
+  if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (G * P + 1), smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return MMVQ_ERR_CUDA;
+  const GroupedCfg best = {G, P, S, per_sm, smem};
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = best;
+  *out = best;
+  return MMVQ_OK;
+}
+
+// CM, the positions per pass, is min(8, n_xq_cols) rounded up to 1, 2, 4
+// or 8 (one kernel instance each): a group rarely holds more positions than
+// there are activation columns, and a larger one is simply processed in
+// more passes.  Active groups are estimated as min(n_groups, n_xq_cols)
+// when the positions index the columns directly, else
+// min(n_groups, 8 n_xq_cols) (a top-8 routing of n_xq_cols tokens); the
+// estimate only steers the shape.
+template <int LAYOUT, int CM>
+static int launch_grouped_tma_cm(const uint8_t* W, int n_experts, int64_t rows, int K,
+                                 const int32_t* expert_ids, const int32_t* offsets, int n_groups,
+                                 const int32_t* act_index, const uint8_t* xq, int n_xq_cols,
+                                 float* y, int32_t* status, cudaStream_t stream) {
+  const int64_t est_active = std::max<int64_t>(
+      1, std::min<int64_t>(n_groups, act_index ? (int64_t)8 * n_xq_cols : (int64_t)n_xq_cols));
+  GroupedCfg cfg;
+  const int rc = grouped_config<LAYOUT, CM>(rows, K, est_active, &cfg);
+  if (rc != MMVQ_OK) return rc;
+  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
+  const int64_t max_items = (int64_t)n_groups * ((n_rg + cfg.G - 1) / cfg.G);
+  const int grid = (int)std::max<int64_t>(
+      1, std::min<int64_t>(max_items, (int64_t)device_sms() * cfg.per_sm));
+  return launch_pdl(mmvq_grouped_tma_kernel<LAYOUT, CM>, dim3(grid),
+                    dim3(32 * (cfg.G * cfg.P + 1)), cfg.smem, stream, W, n_experts, rows, K,
+                    expert_ids, offsets, n_groups, act_index, xq, n_xq_cols, y, status, cfg.S,
+                    cfg.G, cfg.P);
+}
+
+template <int LAYOUT>
+static int launch_grouped_tma_t(const uint8_t* W, int n_experts, int64_t rows, int K,
+                                const int32_t* expert_ids, const int32_t* offsets, int n_groups,
+                                const int32_t* act_index, const uint8_t* xq, int n_xq_cols,
+                                float* y, int32_t* status, cudaStream_t s) {
+  if (n_xq_cols <= 1)
+    return launch_grouped_tma_cm<LAYOUT, 1>(W, n_experts, rows, K, expert_ids, offsets,
+                                            n_groups, act_index, xq, n_xq_cols, y, status, s);
+  if (n_xq_cols == 2)
+    return launch_grouped_tma_cm<LAYOUT, 2>(W, n_experts, rows, K, expert_ids, offsets,
+                                            n_groups, act_index, xq, n_xq_cols, y, status, s);
+  if (n_xq_cols <= 4)
+    return launch_grouped_tma_cm<LAYOUT, 4>(W, n_experts, rows, K, expert_ids, offsets,
+                                            n_groups, act_index, xq, n_xq_cols, y, status, s);
+  return launch_grouped_tma_cm<LAYOUT, 8>(W, n_experts, rows, K, expert_ids, offsets, n_groups,
+                                          act_index, xq, n_xq_cols, y, status, s);
+}
+
+int launch_grouped_tma(int type, const void* W, int n_experts, int64_t rows, int K,
+                       const int32_t* expert_ids, const int32_t* offsets, int n_groups,
+                       const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
+                       int32_t* status, cudaStream_t s) {
+  const uint8_t* w = static_cast<const uint8_t*>(W);
+  const uint8_t* x = static_cast<const uint8_t*>(xq);
+  if (type == MMVQ_Q4_K_PLANAR)
+    return launch_grouped_tma_t<kQ4Planar>(w, n_experts, rows, K, expert_ids, offsets, n_groups,
+                                           act_index, x, n_xq_cols, y, status, s);
+  return launch_grouped_tma_t<kQ6Planar>(w, n_experts, rows, K, expert_ids, offsets, n_groups,
+                                         act_index, x, n_xq_cols, y, status, s);
 }
 
 // Reads and clears the device fault word (after synchronising `stream`).

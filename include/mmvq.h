@@ -160,8 +160,8 @@ MMVQ_API int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K,
  * Grouped expert MMVQ over per-expert token lists (PR #2746 "B70
  * validation": grouped calls with empty groups; issue #2801: the grouped
  * gate/up and down kernels).  W_experts: n_experts matrices of rows x K,
- * one after another, of `type` (MMVQ_Q4_K, MMVQ_Q6_K, or MMVQ_Q4_K_PLANAR
- * with each expert repacked on its own, rows a multiple of 16).  Group g (0 <= g < n_groups) multiplies
+ * one after another, of `type` (MMVQ_Q4_K, MMVQ_Q6_K, or a planar type
+ * with each expert repacked on its own and rows a multiple of 16).  Group g (0 <= g < n_groups) multiplies
  * expert expert_ids[g] with the activation columns of positions
  * p in [token_offsets[g], token_offsets[g+1]); column act_index[p] of xq
  * (column p when act_index == NULL).  Output row p: y[p][0..rows).

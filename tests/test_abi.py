@@ -84,7 +84,8 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_quantize_q8_1(A, 64, 0, 64, A, None) == mmvq.ERR_SHAPE
     g = (12, A, 256, 1536, 2560, A, A, 256, A, A, 1, A, None, None)
     assert L.mmvq_grouped(1012, A, 256, 1530, 2560, A, A, 256, A, A, 1, A, None, None) == mmvq.ERR_SHAPE
-    assert L.mmvq_grouped(*g[:0], 14 + 1000, *g[1:]) == mmvq.ERR_TYPE
+    assert L.mmvq_grouped(1014, A, 256, 1530, 2560, A, A, 256, A, A, 1, A, None, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_grouped(*g[:0], 99, *g[1:]) == mmvq.ERR_TYPE
     assert L.mmvq_grouped(*g[:7], 0, *g[8:]) == mmvq.ERR_ROUTING
     assert L.mmvq_grouped(*g[:7], 4097, *g[8:]) == mmvq.ERR_ROUTING
     assert L.mmvq_grouped(*g[:4], 2560 + 32, *g[5:]) == mmvq.ERR_SHAPE

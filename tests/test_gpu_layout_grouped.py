@@ -66,18 +66,26 @@ def test_route_groups_bit_exact(T, k, E):
     assert host(status)[0] == 0
 
 
+def _experts_on_device(kind, W):
+    """GGUF experts as they are, planar kinds repacked one expert at a time."""
+    if not kind.endswith("_planar"):
+        return dev(W)
+    E, rows, nb, _ = W.shape
+    t = mmvq.TYPE_Q4_K if kind.startswith("q4") else mmvq.TYPE_Q6_K
+    return torch.cat([mmvq.repack_planar(dev(W[e]), rows, nb * 256, type_=t) for e in range(E)])
+
+
 def _grouped_case(kind, T, k, E, rows, K, salt):
     t = {"q4_k": (mmvq.TYPE_Q4_K, oracle.TYPE_Q4_K), "q6_k": (mmvq.TYPE_Q6_K, oracle.TYPE_Q6_K),
-         "q4_k_planar": (mmvq.TYPE_Q4_K_PLANAR, oracle.TYPE_Q4_K)}[kind]
+         "q4_k_planar": (mmvq.TYPE_Q4_K_PLANAR, oracle.TYPE_Q4_K),
+         "q6_k_planar": (mmvq.TYPE_Q6_K_PLANAR, oracle.TYPE_Q6_K)}[kind]
     W = synth.expert_weights(kind.replace("_planar", ""), E, rows, K, salt=salt)
     topk = synth.routing(T, k, E, salt=salt)
     eids, offs, act, _ = oracle.route_groups(topk, E)
     x = synth.activations(K, T, salt=salt)
     xq = oracle.quantize_q8_1(x)
     y_ref, bound = oracle.grouped(t[1], W, E, rows, K, eids, offs, act, xq, with_bound=True)
-    Wd = dev(W)
-    if kind == "q4_k_planar":
-        Wd = torch.cat([mmvq.repack_planar(dev(W[e]), rows, K, type_=mmvq.TYPE_Q4_K) for e in range(E)])
+    Wd = _experts_on_device(kind, W)
     xqd = mmvq.quantize_q8_1(dev(x))
     g_eids, g_offs, g_act, _, _ = mmvq.route_groups(dev(topk), E)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -85,8 +93,8 @@ def _grouped_case(kind, T, k, E, rows, K, salt):
     return host(y), y_ref, bound, host(status)[0]
 
 
-@pytest.mark.parametrize("kind", ["q4_k", "q4_k_planar"])
-@pytest.mark.parametrize("T", [1, 4, 8])
+@pytest.mark.parametrize("kind", ["q4_k", "q4_k_planar", "q6_k_planar"])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_grouped_gate_up_shape(kind, T):
     # 256 experts, gate|up 1536 x 2560, top-8 distinct experts per token
     y, y_ref, bound, st = _grouped_case(kind, T, 8, 256, 1536, 2560, salt=T)
@@ -115,7 +123,8 @@ def test_grouped_down_shape(T, planar):
     assert_within_bound(host(y), y_ref, bound, f"down T={T}")
 
 
-@pytest.mark.parametrize("kind,rows", [("q4_k", 37), ("q6_k", 37), ("q4_k_planar", 48)])
+@pytest.mark.parametrize("kind,rows", [("q4_k", 37), ("q6_k", 37), ("q4_k_planar", 48),
+                                       ("q6_k_planar", 48)])
 def test_grouped_groups_larger_than_eight_and_ragged_rows(kind, rows):
     # 4 experts, 20 tokens, top-2: groups of about 10 positions (processed 8 at a time)
     y, y_ref, bound, st = _grouped_case(kind, 20, 2, 4, rows, 512, salt=3)
@@ -123,30 +132,49 @@ def test_grouped_groups_larger_than_eight_and_ragged_rows(kind, rows):
     assert_within_bound(y, y_ref, bound, kind)
 
 
-def test_grouped_all_groups_empty_writes_nothing():
+_KIND_TYPE = {"q4_k": mmvq.TYPE_Q4_K, "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR,
+              "q6_k_planar": mmvq.TYPE_Q6_K_PLANAR}
+
+
+@pytest.mark.parametrize("kind", ["q4_k", "q4_k_planar", "q6_k_planar"])
+def test_grouped_all_groups_empty_writes_nothing(kind):
     E, rows, K = 8, 32, 256
-    W = dev(synth.expert_weights("q4_k", E, rows, K))
+    W = _experts_on_device(kind, synth.expert_weights(kind[:4], E, rows, K))
     xqd = mmvq.quantize_q8_1(dev(synth.activations(K, 1)))
     eids = torch.arange(E, dtype=torch.int32, device="cuda")
     offs = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
     out = torch.full((4, rows), 7.0, device="cuda")
-    mmvq.grouped(mmvq.TYPE_Q4_K, W, E, rows, K, eids, offs, None, xqd, 1, 4, out=out)
+    mmvq.grouped(_KIND_TYPE[kind], W, E, rows, K, eids, offs, None, xqd, 1, 4, out=out)
     assert np.all(host(out) == 7.0)
 
 
-def test_grouped_flags_bad_routing_without_faulting():
+@pytest.mark.parametrize("kind", ["q4_k", "q4_k_planar", "q6_k_planar"])
+def test_grouped_flags_bad_routing_without_faulting(kind):
     E, rows, K = 4, 32, 256
-    W = dev(synth.expert_weights("q4_k", E, rows, K))
+    W = _experts_on_device(kind, synth.expert_weights(kind[:4], E, rows, K))
     xqd = mmvq.quantize_q8_1(dev(synth.activations(K, 3)))
     eids = dev(np.array([0, 9, 2], np.int32))           # expert 9 does not exist
     offs = dev(np.array([0, 1, 2, 3], np.int32))
     act = dev(np.array([0, 1, 5], np.int32))            # column 5 does not exist
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.full((3, rows), 7.0, device="cuda")
-    mmvq.grouped(mmvq.TYPE_Q4_K, W, E, rows, K, eids, offs, act, xqd, 3, 3, out=out,
+    mmvq.grouped(_KIND_TYPE[kind], W, E, rows, K, eids, offs, act, xqd, 3, 3, out=out,
                  status=status)
     o = host(out)
     assert host(status)[0] == mmvq.ERR_ROUTING
     assert np.all(o[1] == 7.0)                           # skipped group
     assert np.all(o[2] == 0.0)                           # zero activation column
     assert np.any(o[0] != 7.0)
+
+
+@pytest.mark.parametrize("kind", ["q4_k_planar", "q6_k_planar"])
+def test_grouped_planar_is_bitwise_repeatable(kind):
+    # fixed reduction order: the same call gives the same bits every time
+    E, rows, K, T, k = 32, 512, 2560, 8, 8
+    W = _experts_on_device(kind, synth.expert_weights(kind[:4], E, rows, K, salt=5))
+    topk = synth.routing(T, k, E, salt=5)
+    xqd = mmvq.quantize_q8_1(dev(synth.activations(K, T, salt=5)))
+    g_eids, g_offs, g_act, _, _ = mmvq.route_groups(dev(topk), E)
+    outs = [host(mmvq.grouped(_KIND_TYPE[kind], W, E, rows, K, g_eids, g_offs, g_act, xqd, T,
+                              T * k)) for _ in range(3)]
+    assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
