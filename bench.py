@@ -92,9 +92,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(summary: str):
-    """DRAM bytes per MMVQ launch from a committed ncu summary, or None when
-    the summary is missing or was taken on different kernel sources."""
+def profiled_field(summary: str, key: str):
+    """A number from a committed ncu summary, or None when the summary is
+    missing or was taken on different kernel sources."""
     try:
         text = open(os.path.join(HERE, "profiles", summary)).read()
     except OSError:
@@ -103,9 +103,15 @@ def profiled_traffic(summary: str):
     if fields.get("kernel_source_sha256", "").strip() != kernel_source_hash():
         return None
     try:
-        return int(fields["traffic_bytes_per_mmvq_launch"])
+        return float(fields[key])
     except (KeyError, ValueError):
         return None
+
+
+def profiled_traffic(summary: str):
+    """DRAM bytes per MMVQ launch from a committed ncu summary (or None)."""
+    v = profiled_field(summary, "traffic_bytes_per_mmvq_launch")
+    return None if v is None else int(v)
 
 
 def load_peak():
@@ -268,8 +274,11 @@ def run_ours(args, rank, world, local_rank):
     y_pinned = torch.empty(y_total, dtype=torch.float32).pin_memory()
     calls_of_case = [[i for i, c in enumerate(calls) if c[0] == ci] for ci in range(len(case_list))]
 
-    def run_case(ci, s=None, evs=None):
-        """Quantise the case's columns once, then every copy's MMVQ back to back."""
+    def run_case(ci, s=None, evs=None, dependent=False):
+        """Quantise the case's columns once, then every copy's MMVQ back to back.
+        dependent=True drops the stable-activation flag: every call then waits
+        for its predecessor before it stages the activations (a chain of
+        calls that each consume the previous result)."""
         si, fmt, rows, K, nc, xo = case_list[ci]
         if evs is not None:
             _record_external(evs[3 * ci], s)
@@ -281,7 +290,7 @@ def run_ours(args, rank, world, local_rank):
             # after the first call no kernel that may still run writes xq
             mmvq.gemv(type_of[fmt], mats[si][cp], rows, K, xq_bufs[ci], nc,
                       out=y_dev[yo:yo + nc * rows].view(nc, rows),
-                      flags=mmvq.FLAG_XQ_STABLE if n else 0)
+                      flags=mmvq.FLAG_XQ_STABLE if (n and not dependent) else 0)
         if evs is not None:
             _record_external(evs[3 * ci + 2], s)
 
@@ -342,6 +351,27 @@ def run_ours(args, rank, world, local_rank):
     g_us = np.array([evs[3 * ci + 1].elapsed_time(evs[3 * ci + 2]) * 1e3
                      for ci in range(len(case_list))])
 
+    # the same calls as a dependent chain (outside the timed region): median
+    # over a few replays of a second graph
+    evd = [torch.cuda.Event(enable_timing=True) for _ in range(3 * len(case_list))]
+    for e in evd:
+        e.record()
+    torch.cuda.synchronize()
+    graph_dep = torch.cuda.CUDAGraph()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph_dep, stream=cap, capture_error_mode="thread_local"):
+        s = torch.cuda.current_stream()
+        for ci in range(len(case_list)):
+            run_case(ci, s, evd, dependent=True)
+    torch.cuda.synchronize()
+    dep_runs = []
+    for _ in range(5):
+        graph_dep.replay()
+        torch.cuda.synchronize()
+        dep_runs.append([evd[3 * ci + 1].elapsed_time(evd[3 * ci + 2]) * 1e3
+                         for ci in range(len(case_list))])
+    d_us = np.median(np.array(dep_runs), axis=0)
+
     peak, peak_kind = load_peak()
     w_step = 0
     alg_step = 0
@@ -352,11 +382,14 @@ def run_ours(args, rank, world, local_rank):
         w_step += wb * n
         alg_step += metrics.call_bytes(fmt, rows, K, nc) * n
         gu = float(g_us[ci]) / n
+        du = float(d_us[ci]) / n
         per_case.append({"shape": f"{rows}x{K}", "fmt": fmt, "ncols": nc, "calls": n,
                          "launch": mmvq.launch_shape(type_of[fmt], rows, K, nc),
                          "us_per_call": round(gu, 3), "us_quantize": round(float(q_us[ci]), 3),
                          "weight_gbps": round(wb / gu / 1e3, 1),
-                         "frac_of_measured": round(wb / gu / 1e3 / peak, 3)})
+                         "frac_of_measured": round(wb / gu / 1e3 / peak, 3),
+                         "us_per_call_dependent": round(du, 3),
+                         "weight_gbps_dependent": round(wb / du / 1e3, 1)})
     step_s = elapsed_ms / 1e3 / args.steps
     value = world * w_step / step_s / 1e9
     achieved = alg_step / (float(np.sum(g_us)) * 1e-6) / 1e9
@@ -385,6 +418,9 @@ def run_ours(args, rank, world, local_rank):
                    "weight_copies": [len(m) for m in mats],
                    "l2": "weights rotated over copies > 2x L2 per shape (inputs larger than L2)",
                    "timing": "CUDA graph replay of the step; event nodes at case boundaries",
+                   "chain": "calls after a case's first carry the stable-activation flag, so "
+                            "consecutive calls overlap; *_dependent per case: the same calls "
+                            "without it (each waits for its predecessor), timed after the step",
                    "step": "per case: Q8_1-quantise its columns once, then one MMVQ per weight copy",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -400,6 +436,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": (len(calls) + len(case_list)) * args.steps,
         "clocks": clk,
         "cases": per_case,
+        "dependent_chain": {"weight_gbps": round(w_step / (float(np.sum(d_us)) * 1e-6) / 1e9, 1),
+                            "mmvq_us_per_step": round(float(np.sum(d_us)), 1),
+                            "note": "MMVQ launches only, each call waiting for the previous"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cases_spec, host_weights, args.cpu_seconds)
@@ -524,6 +563,10 @@ def run_moe(args, rank, world, local_rank):
     dn_bytes = np.mean([d * metrics.weight_bytes("q4_k", H, F) for d in distinct])
     peak, peak_kind = load_peak()
     achieved = gu_bytes / (mean_us[2] * 1e-6) / 1e9
+    # DRAM bytes per gate|up launch: the profiled traffic / weight-byte ratio
+    # (T=8 capture) applied to this run's mean weight bytes per launch
+    ratio = profiled_field("mmvq_grouped_moe_t8.md", "traffic_over_weight_bytes_gate_up")
+    gu_traffic = None if ratio is None else round(ratio * gu_bytes)
 
     e2e_steps = max(3, min(args.steps, 200))
     torch.cuda.synchronize()
@@ -546,7 +589,8 @@ def run_moe(args, rank, world, local_rank):
                    "timing": "CUDA graph replay of whole steps; per-kernel times from a "
                              "second graph with event nodes between the five kernels"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 3), "traffic": None,
+                     "frac": round(achieved / peak, 3), "traffic": gu_traffic,
+                     "algorithmic_bytes_per_launch": round(gu_bytes),
                      "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "grouped gate|up MMVQ"},
         "e2e": {"value": round(np.mean(step_bytes) / e2e_s / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y.numel() * 4),
