@@ -18,6 +18,7 @@ int launch_repack_planar(int type, const void* W, int64_t rows, int K, void* P, 
 int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_ids, int n,
                          void* out, int32_t* status, cudaStream_t s);
 int read_device_fault(int* fault, cudaStream_t stream);
+int launch_wait_timeout_selftest(uint32_t limit_us, cudaStream_t stream);
 int dense_shape(int type, int64_t rows, int K, int ncols, int32_t* info);
 int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
                         int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
@@ -181,6 +182,11 @@ int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
   if (rc) return rc;
   if (ncols < 1 || ncols > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
   return mmvq::dense_shape(type, rows, K, ncols, info);
+}
+
+int mmvq_selftest_wait_timeout(unsigned int limit_us, mmvq_stream_t stream) {
+  if (limit_us < 1 || limit_us > 100000) return MMVQ_ERR_SHAPE;
+  return mmvq::launch_wait_timeout_selftest(limit_us, (cudaStream_t)stream);
 }
 
 int mmvq_read_device_fault(int* fault, mmvq_stream_t stream) {

@@ -72,10 +72,12 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Waits for the phase with the given parity to complete; false after ~1 s.
-// The timer is read once every 64 tries; `backoff_ns` > 0 sleeps between
-// tries (the producer, whose waits are not on the critical path).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int backoff_ns = 0) {
+// Waits for the phase with the given parity to complete; false once
+// `limit_ns` (about 1 s by default) has passed.  The timer is read once every
+// 64 tries; `backoff_ns` > 0 sleeps between tries (the producer, whose waits
+// are not on the critical path).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int backoff_ns = 0,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
@@ -85,7 +87,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int ba
       const uint64_t t = global_ns();
       if (t0 == 0) {
         t0 = t;
-      } else if (t - t0 > kWaitLimitNs) {
+      } else if (t - t0 > limit_ns) {
         return false;
       }
     }
@@ -935,6 +937,25 @@ int launch_grouped_tma(int type, const void* W, int n_experts, int64_t rows, int
                                            act_index, x, n_xq_cols, y, status, s);
   return launch_grouped_tma_t<kQ6Planar>(w, n_experts, rows, K, expert_ids, offsets, n_groups,
                                          act_index, x, n_xq_cols, y, status, s);
+}
+
+// Self-test of the bounded waits: one warp waits on a shared-memory barrier
+// that nothing completes, with the kernels' own wait routine and a short
+// limit, and reports the timeout through the fault word as they do.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0u, 0, limit_ns))
+    atomicOr(&g_fault_word, kFaultMbarTimeout);
+}
+
+int launch_wait_timeout_selftest(uint32_t limit_us, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>((uint64_t)limit_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
 }
 
 // Reads and clears the device fault word (after synchronising `stream`).

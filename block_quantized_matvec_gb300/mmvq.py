@@ -44,6 +44,7 @@ SIGNATURES = {
     "mmvq_repack_planar": (_I, [_I, _P, _I64, _I, _P, _P]),
     "mmvq_gather_planar_rows": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P]),
     "mmvq_read_device_fault": (_I, [_P, _P]),
+    "mmvq_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "mmvq_launch_shape": (_I, [_I, _I64, _I, _I, _P]),
 }
 
@@ -207,6 +208,12 @@ def read_device_fault(stream=None) -> int:
     v = ctypes.c_int(0)
     _check(lib().mmvq_read_device_fault(ctypes.byref(v), _stream(stream)), "mmvq_read_device_fault")
     return v.value
+
+
+def selftest_wait_timeout(limit_us: int = 2000, stream=None) -> None:
+    """Run one bounded barrier wait to expiry (sets bit 1 of the fault word)."""
+    _check(lib().mmvq_selftest_wait_timeout(limit_us, _stream(stream)),
+           "mmvq_selftest_wait_timeout")
 
 
 def planar_bytes(rows: int, K: int, type_: int = TYPE_Q6_K) -> int:

@@ -246,6 +246,16 @@ MMVQ_API int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t
  */
 MMVQ_API int mmvq_read_device_fault(int* fault, mmvq_stream_t stream);
 
+/*
+ * Self-test of the bounded waits above: launches one warp that waits, with
+ * the kernels' own wait routine and a limit of limit_us microseconds
+ * (1..100000), on a shared-memory barrier that nothing completes.  The wait
+ * runs out and sets bit 1 of the device fault word, read afterwards with
+ * mmvq_read_device_fault; nothing faults and the context stays usable.  For
+ * checking the failure path on a live GPU; no counterpart on the pages.
+ */
+MMVQ_API int mmvq_selftest_wait_timeout(unsigned int limit_us, mmvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

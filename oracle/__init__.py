@@ -72,6 +72,7 @@ def _load():
             lib.orc_route_groups.argtypes = [P, I, I, I, P, P, P, P]
             lib.orc_grouped.argtypes = [I, P, I, I64, I, P, P, I, P, P, P, P]
             lib.orc_silu_mul_quantize.argtypes = [P, I, I, P, P]
+            lib.orc_rmsnorm_quantize_q8_1.argtypes = [P, P, ctypes.c_float, I, I, I64, P, P]
             _lib = lib
     return _lib
 
@@ -228,3 +229,17 @@ def silu_mul_quantize(gu: np.ndarray, F: int):
     h = np.empty((n, F), dtype=np.float32)
     _check(_load().orc_silu_mul_quantize(_p(gu), F, n, _p(xq), _p(h)), "silu_mul_quantize")
     return xq, h
+
+
+def rmsnorm_quantize_q8_1(x: np.ndarray, w: np.ndarray, eps: float):
+    """x [ncols, K], w [K] -> (xq [ncols, K/32, 36], y [ncols, K]) of RMSNorm(x) * w."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    ncols, K = x.shape
+    xq = np.empty((ncols, K // 32, Q81_BYTES), dtype=np.uint8)
+    y = np.empty((ncols, K), dtype=np.float32)
+    _check(_load().orc_rmsnorm_quantize_q8_1(_p(x), _p(w), eps, K, ncols, K, _p(xq), _p(y)),
+           "rmsnorm_quantize_q8_1")
+    return xq, y

@@ -33,6 +33,9 @@
 //    (PR #2746 "B70 validation": "empty groups"; issue #2801: the grouped
 //    gate/up and down kernels), and SiLU(gate)*up requantised to Q8_1
 //    between the gate/up and down calls.
+//  * RMSNorm folded into the Q8_1 quantiser (PR #1774 "How it was checked" names the
+//    opt-in fused norm, #1775, without a formula): the plain RMS norm with a
+//    weight vector, mean square accumulated in fp64.
 //
 // Floating point: compiled with -O2 -ffp-contract=off, so every a*b+c below
 // is two roundings, exactly as written.
@@ -584,6 +587,33 @@ int orc_grouped(int type, const uint8_t* W, int n_experts, int64_t rows, int K,
 
 // gu: [n][2F] rows laid out [gate F | up F].  h = g/(1+exp(-g)) * u in fp32,
 // then Q8_1 per 32 into xq [n][F/32].  h_out (may be NULL): [n][F].
+// RMSNorm then Q8_1, per column: the step before the activation quantiser
+// when the norm is folded into it ("Strata" PR #1774 "How it was checked": the opt-in
+// STRATA_GR_FUSE_NORM, #1775; the pages give no formula, so this is the
+// plain RMS norm with a weight vector).  ms = (sum x_i^2 in fp64, index
+// order) / K; scale = fp32(1 / sqrt(ms + eps)) in fp64; y_i = (x_i * scale)
+// * w_i in fp32 (two roundings); then Q8_1 of y as orc_quantize_q8_1.
+int orc_rmsnorm_quantize_q8_1(const float* x, const float* w, float eps, int K, int ncols,
+                              int64_t ldx, uint8_t* xq, float* y_out) {
+  if (K <= 0 || K % kQK8 != 0 || ncols < 0 || ldx < K || !(eps >= 0.0f)) return -2;
+  const int nbq = K / kQK8;
+  std::vector<float> y((size_t)K);
+  for (int c = 0; c < ncols; ++c) {
+    const float* xc = x + (int64_t)c * ldx;
+    double ss = 0.0;
+    for (int i = 0; i < K; ++i) ss += (double)xc[i] * (double)xc[i];
+    const float scale = (float)(1.0 / std::sqrt(ss / (double)K + (double)eps));
+    for (int i = 0; i < K; ++i) {
+      const float t = xc[i] * scale;
+      y[i] = t * w[i];
+    }
+    if (y_out) std::memcpy(y_out + (int64_t)c * K, y.data(), sizeof(float) * K);
+    for (int kb = 0; kb < nbq; ++kb)
+      quantize_block_q8_1(y.data() + kb * kQK8, xq + ((int64_t)c * nbq + kb) * kQ81Bytes);
+  }
+  return 0;
+}
+
 int orc_silu_mul_quantize(const float* gu, int F, int n, uint8_t* xq, float* h_out) {
   if (F <= 0 || F % kQK8 != 0 || n < 0) return -2;
   std::vector<float> h((size_t)F);

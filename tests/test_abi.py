@@ -91,6 +91,8 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_grouped(*g[:4], 2560 + 32, *g[5:]) == mmvq.ERR_SHAPE
     assert L.mmvq_grouped(*g[:5], None, *g[6:]) == mmvq.ERR_NULL
     assert L.mmvq_grouped(*g[:9], A + 4, *g[10:]) == mmvq.ERR_ALIGN
+    assert L.mmvq_selftest_wait_timeout(0, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_selftest_wait_timeout(100001, None) == mmvq.ERR_SHAPE
     assert L.mmvq_route_groups(A, 4, 8, 0, A, A, A, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_route_groups(A, 10000, 8, 256, A, A, A, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_route_groups(None, 4, 8, 256, A, A, A, A, None, None) == mmvq.ERR_NULL
