@@ -76,15 +76,19 @@ WORKLOAD_DESC = {
     "moe_t1": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=1 top-8 (planar experts)",
     "moe_t4": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=4 top-8 (planar experts)",
     "moe_t8": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=8 top-8 (planar experts)",
+    "prologue": "RMSNorm folded into the Q8_1 quantiser vs the plain quantiser, K = 2560 and 10240 at 1, 4, 8 cols",
 }
 
 
+MMVQ_SOURCES = ["api.cu", "common.cuh", "kquant.cuh", "mmvq_dense.cu", "mmvq_tma.cu", "rowgroup.cuh"]
+
+
 def kernel_source_hash() -> str:
-    """sha256 of the CUDA sources and the ABI header (the kernels as built)."""
-    import glob
+    """sha256 of the sources the profiled MMVQ kernels (dense ring, grouped
+    ring, their launch choosers) are built from, and of the ABI header."""
     import hashlib
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(HERE, "block_quantized_matvec_gb300", "csrc", "*"))) + \
+    for p in [os.path.join(HERE, "block_quantized_matvec_gb300", "csrc", f) for f in MMVQ_SOURCES] + \
             [os.path.join(HERE, "include", "mmvq.h")]:
         h.update(os.path.basename(p).encode())
         with open(p, "rb") as f:
@@ -603,6 +607,72 @@ def run_moe(args, rank, world, local_rank):
     }
     return out
 
+# ------------------------------------------------ activation prologue --
+
+def run_prologue(args, rank, world, local_rank):
+    """Per call: RMSNorm + Q8_1 of ncols columns (x and w read, Q8_1 written)
+    against the plain Q8_1 quantiser of the same columns; CUDA graphs of
+    back-to-back calls, inputs L2-resident (they are a few hundred KB)."""
+    import torch
+    from block_quantized_matvec_gb300 import mmvq, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    mmvq.lib()
+    n_calls = 200
+    cases = []
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    clocks.wait_first_sample()
+    clocks.mark()
+    total_bytes, total_s = 0.0, 0.0
+    for K in (2560, 10240):
+        w = torch.from_numpy(synth.activations(K, 1, salt=K)[0]).to(dev)
+        for nc in (1, 4, 8):
+            x = torch.from_numpy(synth.activations(K, nc, salt=K + nc)).to(dev)
+            xq = torch.empty((nc, K // 32, 36), dtype=torch.uint8, device=dev)
+            row = {"K": K, "ncols": nc}
+            for name, fn in (("rmsnorm_q8_1", lambda: mmvq.rmsnorm_quantize_q8_1(x, w, 1e-6, out=xq)),
+                             ("q8_1", lambda: mmvq.quantize_q8_1(x, out=xq))):
+                fn()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream(device=dev)
+                cap.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                    for _ in range(n_calls):
+                        fn()
+                for _ in range(max(3, args.warmup)):
+                    g.replay()
+                torch.cuda.synchronize()
+                reps = 5
+                t0 = torch.cuda.Event(enable_timing=True)
+                t1 = torch.cuda.Event(enable_timing=True)
+                t0.record()
+                for _ in range(reps):
+                    g.replay()
+                t1.record()
+                torch.cuda.synchronize()
+                us = t0.elapsed_time(t1) * 1e3 / (reps * n_calls)
+                row[f"us_{name}"] = round(us, 3)
+                if name == "rmsnorm_q8_1":
+                    nbytes = 4 * K * nc + 4 * K + 36 * (K // 32) * nc
+                    total_bytes += nbytes * reps * n_calls
+                    total_s += us * 1e-6 * reps * n_calls
+            cases.append(row)
+    clk = clocks.stop()
+    return {
+        "metric": "RMSNorm+Q8_1 prologue: bytes moved (x, w in; Q8_1 out) per second",
+        "value": round(total_bytes / total_s / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": n_calls, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp64 mean square + fp32",
+        "data": "synthetic N(0,1) columns and weights",
+        "config": {"workload": WORKLOAD_DESC["prologue"], "eps": 1e-6,
+                   "timing": "CUDA graph of 200 back-to-back calls, 5 replays"},
+        "gpu_launches": len(cases) * 2 * n_calls * 5, "clocks": clk, "cases": cases,
+    }
+
+
 # ---------------------------------------------------------- CPU oracle --
 
 def _oracle_pass(cases_spec, host_weights, row_sample, salt0=0):
@@ -735,6 +805,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if args.workload.startswith("moe_"):
         res = run_moe(args, rank, world, local_rank)
+    elif args.workload == "prologue":
+        res = run_prologue(args, rank, world, local_rank)
     else:
         res = run_ours(args, rank, world, local_rank)
     if rank == 0:

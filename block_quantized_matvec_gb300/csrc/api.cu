@@ -8,6 +8,8 @@
 namespace mmvq {
 int launch_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq, cudaStream_t s);
 int launch_silu_mul_quantize(const float* gu, int F, int n, void* xq, float* h_out, cudaStream_t s);
+int launch_rmsnorm_quantize(const float* x, const float* w, float eps, int K, int ncols,
+                            int64_t ldx, void* xq, float* y_out, cudaStream_t s);
 int launch_dense(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
                  int32_t* sumi, uint32_t flags, cudaStream_t s);
 int launch_grouped(int type, const void* W, int n_experts, int64_t rows, int K,
@@ -187,6 +189,17 @@ int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
 int mmvq_selftest_wait_timeout(unsigned int limit_us, mmvq_stream_t stream) {
   if (limit_us < 1 || limit_us > 100000) return MMVQ_ERR_SHAPE;
   return mmvq::launch_wait_timeout_selftest(limit_us, (cudaStream_t)stream);
+}
+
+int mmvq_rmsnorm_quantize_q8_1(const float* x, const float* w, float eps, int K, int ncols,
+                               int64_t ldx, void* xq, float* y_out, mmvq_stream_t stream) {
+  if (!x || !w || !xq) return MMVQ_ERR_NULL;
+  if (K <= 0 || K % mmvq::kQK8 != 0 || K > (1 << 24) || ncols < 1 || ncols > 65535 || ldx < K)
+    return MMVQ_ERR_SHAPE;
+  if (!(eps >= 0.0f) || !(eps < INFINITY)) return MMVQ_ERR_SHAPE;
+  if (!aligned(x, 4) || !aligned(w, 4) || !aligned(xq, 16) || (y_out && !aligned(y_out, 4)))
+    return MMVQ_ERR_ALIGN;
+  return mmvq::launch_rmsnorm_quantize(x, w, eps, K, ncols, ldx, xq, y_out, (cudaStream_t)stream);
 }
 
 int mmvq_read_device_fault(int* fault, mmvq_stream_t stream) {

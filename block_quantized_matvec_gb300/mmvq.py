@@ -45,6 +45,7 @@ SIGNATURES = {
     "mmvq_gather_planar_rows": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P]),
     "mmvq_read_device_fault": (_I, [_P, _P]),
     "mmvq_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
+    "mmvq_rmsnorm_quantize_q8_1": (_I, [_P, _P, ctypes.c_float, _I, _I, _I64, _P, _P, _P]),
     "mmvq_launch_shape": (_I, [_I, _I64, _I, _I, _P]),
 }
 
@@ -208,6 +209,28 @@ def read_device_fault(stream=None) -> int:
     v = ctypes.c_int(0)
     _check(lib().mmvq_read_device_fault(ctypes.byref(v), _stream(stream)), "mmvq_read_device_fault")
     return v.value
+
+
+def rmsnorm_quantize_q8_1(x: torch.Tensor, w: torch.Tensor, eps: float,
+                          out: torch.Tensor | None = None, y_out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """x [ncols, K] fp32 (rows may be strided), w [K] fp32 -> Q8_1 of RMSNorm(x) * w,
+    [ncols, K/32, 36]."""
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    _dev(w, "w")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    ncols, K = x.shape
+    if x.dtype != torch.float32 or w.dtype != torch.float32 or x.stride(1) != 1 or \
+            not w.is_contiguous() or w.numel() != K:
+        raise ValueError("x [ncols, K] with unit inner stride and w [K], both float32")
+    if out is None:
+        out = torch.empty((ncols, K // 32, Q8_1_BYTES), dtype=torch.uint8, device=x.device)
+    _check(lib().mmvq_rmsnorm_quantize_q8_1(_ptr(x), _ptr(w), eps, K, ncols, x.stride(0),
+                                            _ptr(out), _ptr(y_out), _stream(stream)),
+           "mmvq_rmsnorm_quantize_q8_1")
+    return out
 
 
 def selftest_wait_timeout(limit_us: int = 2000, stream=None) -> None:

@@ -201,6 +201,21 @@ MMVQ_API int mmvq_route_groups(const int32_t* topk, int T, int k, int n_experts,
 MMVQ_API int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq, float* h_out,
                                 mmvq_stream_t stream);
 
+/*
+ * RMSNorm folded into the Q8_1 quantiser (the opt-in fused norm named in
+ * PR #1774 "How it was checked"; the pages give no formula, so the plain RMS
+ * norm with a weight vector).  Per column c of x (fp32 [ncols][ldx], ldx >= K):
+ * ms = (sum of x_i^2 in fp64) / K, scale = fp32(1 / sqrt(ms + eps)) computed
+ * in fp64, y_i = (x_i * scale) * w_i in fp32 (w: fp32 [K]), then Q8_1 of y
+ * into xq ([ncols][K/32] blocks) exactly as mmvq_quantize_q8_1.  y_out (may
+ * be NULL): fp32 [ncols][K].  Requires K % 32 == 0, 0 < K <= 2^24,
+ * 1 <= ncols <= 65535, 0 <= eps < inf; x, w, y_out 4-byte and xq 16-byte
+ * aligned.
+ */
+MMVQ_API int mmvq_rmsnorm_quantize_q8_1(const float* x, const float* w, float eps, int K, int ncols,
+                                        int64_t ldx, void* xq, float* y_out,
+                                        mmvq_stream_t stream);
+
 /* Bytes of the planar form of a rows x K matrix of `type` (MMVQ_Q6_K or
  * MMVQ_Q4_K); -1 on a bad type or shape. */
 MMVQ_API int64_t mmvq_planar_bytes(int type, int64_t rows, int K);

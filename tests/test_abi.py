@@ -91,6 +91,14 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_grouped(*g[:4], 2560 + 32, *g[5:]) == mmvq.ERR_SHAPE
     assert L.mmvq_grouped(*g[:5], None, *g[6:]) == mmvq.ERR_NULL
     assert L.mmvq_grouped(*g[:9], A + 4, *g[10:]) == mmvq.ERR_ALIGN
+    r = (A, A, 1e-6, 2560, 2, 2560, A, None, None)
+    assert L.mmvq_rmsnorm_quantize_q8_1(None, *r[1:]) == mmvq.ERR_NULL
+    assert L.mmvq_rmsnorm_quantize_q8_1(*r[:3], 2560 + 16, *r[4:]) == mmvq.ERR_SHAPE
+    assert L.mmvq_rmsnorm_quantize_q8_1(*r[:4], 0, *r[5:]) == mmvq.ERR_SHAPE
+    assert L.mmvq_rmsnorm_quantize_q8_1(*r[:5], 2048, *r[6:]) == mmvq.ERR_SHAPE   # ldx < K
+    assert L.mmvq_rmsnorm_quantize_q8_1(*r[:2], -1.0, *r[3:]) == mmvq.ERR_SHAPE
+    assert L.mmvq_rmsnorm_quantize_q8_1(*r[:2], float("nan"), *r[3:]) == mmvq.ERR_SHAPE
+    assert L.mmvq_rmsnorm_quantize_q8_1(*r[:6], A + 4, *r[7:]) == mmvq.ERR_ALIGN
     assert L.mmvq_selftest_wait_timeout(0, None) == mmvq.ERR_SHAPE
     assert L.mmvq_selftest_wait_timeout(100001, None) == mmvq.ERR_SHAPE
     assert L.mmvq_route_groups(A, 4, 8, 0, A, A, A, A, None, None) == mmvq.ERR_SHAPE
