@@ -23,32 +23,6 @@ struct Q6Half {
   uint32_t d;  // fp16 bits in the low half
 };
 
-// Planar tile: every lane load is one aligned 16-byte load and each warp
-// instruction reads one contiguous 512-byte segment.
-__device__ __forceinline__ void load_q6_planar(const uint8_t* __restrict__ tile, int lane,
-                                               Q6Half& w) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 v = ldg_nc_v4(tile + 512 * j + 16 * lane);
-    w.ql[4 * j + 0] = v.x;
-    w.ql[4 * j + 1] = v.y;
-    w.ql[4 * j + 2] = v.z;
-    w.ql[4 * j + 3] = v.w;
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint4 v = ldg_nc_v4(tile + 2048 + 512 * j + 16 * lane);
-    w.qh[4 * j + 0] = v.x;
-    w.qh[4 * j + 1] = v.y;
-    w.qh[4 * j + 2] = v.z;
-    w.qh[4 * j + 3] = v.w;
-  }
-  const uint2 s = ldg_nc_v2(tile + 3072 + 8 * lane);
-  w.sc[0] = s.x;
-  w.sc[1] = s.y;
-  w.d = ldg_nc_u16(tile + 3328 + 2 * (lane & 15));
-}
-
 // GGUF block staged in shared memory at a 2-byte aligned address `blk`:
 // aligned word loads, realigned with a funnel shift when the block starts
 // on an odd half-word.
@@ -134,122 +108,6 @@ __device__ __forceinline__ void q6_dot(const Q6Half& w, int h, int b, const uint
   for (int c = 0; c < NCOLS; ++c) acc[c] = fmaf(dw, inner[c], acc[c]);
 }
 
-// Per-(column, 32-block) activation record in shared memory: d_a, the two
-// offset corrections -32 * (sum of the 16 quants of each half) for the
-// unsigned Q6_K codes, and s_a (Q4_K min term), as one 16-byte load.
-struct ActRec {
-  float d;
-  int corr0;
-  int corr1;
-  float s;
-};
-
-// Stages Q8_1 columns: quants into the padded rows of `act`, d and s into
-// rec[c][kb] (first pass; see stage_q8_1 for the 16-byte vector reads).
-template <typename ColOf>
-__device__ __forceinline__ void stage_q8_1_rec(const uint8_t* __restrict__ xq, int K, int ncols,
-                                               ColOf col_of, uint8_t* act, ActRec* rec, int tid,
-                                               int nthreads) {
-  const int nbq = K / kQK8;
-  const int vec_per_col = nbq * 9 / 4;
-  const int rb = act_row_bytes(K);
-  for (int v = tid; v < ncols * vec_per_col; v += nthreads) {
-    const int c = v / vec_per_col;
-    const int vi = v - c * vec_per_col;
-    const int col = col_of(c);
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    if (col >= 0)
-      q = __ldg(reinterpret_cast<const uint4*>(xq + (size_t)col * nbq * kQ81Bytes) + vi);
-    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int w = 4 * vi + e;
-      const int kb = w / 9;
-      const int k = w - kb * 9;
-      if (k == 0) {
-        rec[c * nbq + kb].d = half_bits_to_float((uint16_t)(w4[e] & 0xffff));
-        rec[c * nbq + kb].s = half_bits_to_float((uint16_t)(w4[e] >> 16));
-      } else {
-        *reinterpret_cast<uint32_t*>(act + c * rb + act_off(kb) + 4 * (k - 1)) = w4[e];
-      }
-    }
-  }
-}
-
-// Second pass (after the quants are visible): the offset corrections
-// -32 * (sum of the 16 quants of each half of every 32-block).
-__device__ __forceinline__ void finish_act_records(const uint8_t* act, int rb, int nbq, int ncols,
-                                                   ActRec* rec, int tid, int nthreads) {
-  for (int v = tid; v < ncols * nbq; v += nthreads) {
-    const int c = v / nbq;
-    const int kb = v - c * nbq;
-    const int4* q = reinterpret_cast<const int4*>(act + c * rb + act_off(kb));
-    const int4 q0 = q[0], q1 = q[1];
-    int s0 = dp4a(q0.x, 0x01010101, 0);
-    s0 = dp4a(q0.y, 0x01010101, s0);
-    s0 = dp4a(q0.z, 0x01010101, s0);
-    s0 = dp4a(q0.w, 0x01010101, s0);
-    int s1 = dp4a(q1.x, 0x01010101, 0);
-    s1 = dp4a(q1.y, 0x01010101, s1);
-    s1 = dp4a(q1.z, 0x01010101, s1);
-    s1 = dp4a(q1.w, 0x01010101, s1);
-    rec[c * nbq + kb].corr0 = -32 * s0;
-    rec[c * nbq + kb].corr1 = -32 * s1;
-  }
-}
-
-// Q6_K with the codes kept unsigned (q in 0..63): sum (q-32)*a is computed as
-// dp4a(q, a) started from -32 * sum(a) per 16 activations, which gives the
-// same integers as subtracting 32 from every code, without any per-code
-// work.  Decode is then three or four word operations per four codes.
-template <int NCOLS>
-__device__ __forceinline__ void q6_dot_u(const Q6Half& w, int h, int b, const uint8_t* act, int rb,
-                                         const ActRec* rec, int nbq, float (&acc)[NCOLS],
-                                         int32_t* sumi_out, int64_t sumi_cs) {
-  float inner[NCOLS];
-#pragma unroll
-  for (int c = 0; c < NCOLS; ++c) inner[c] = 0.0f;
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    int wv[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      uint32_t lo = (r & 1) ? w.ql[8 + m] : w.ql[m];
-      if (r & 2) lo >>= 4;
-      uint32_t hi;
-      if (r == 0) hi = w.qh[m] << 4;
-      else if (r == 1) hi = w.qh[m] << 2;
-      else if (r == 2) hi = w.qh[m];
-      else hi = w.qh[m] >> 2;
-      wv[m] = (int)((lo & 0x0f0f0f0fu) | (hi & 0x30303030u));
-    }
-    const uint32_t scw = w.sc[r >> 1] >> (16 * (r & 1));
-    const int sc0 = sext8(scw), sc1 = sext8(scw >> 8);
-    const int kb = 8 * b + 4 * h + r;
-#pragma unroll
-    for (int c = 0; c < NCOLS; ++c) {
-      const int4* a = reinterpret_cast<const int4*>(act + c * rb + act_off(kb));
-      const int4 a0 = a[0];
-      const int4 a1 = a[1];
-      const ActRec rc = rec[c * nbq + kb];
-      int s0 = dp4a(wv[0], a0.x, rc.corr0);
-      s0 = dp4a(wv[1], a0.y, s0);
-      s0 = dp4a(wv[2], a0.z, s0);
-      s0 = dp4a(wv[3], a0.w, s0);
-      int s1 = dp4a(wv[4], a1.x, rc.corr1);
-      s1 = dp4a(wv[5], a1.y, s1);
-      s1 = dp4a(wv[6], a1.z, s1);
-      s1 = dp4a(wv[7], a1.w, s1);
-      const int sumi = sc0 * s0 + sc1 * s1;
-      if (sumi_out) sumi_out[c * sumi_cs + kb] = sumi;
-      inner[c] = fmaf(rc.d, (float)sumi, inner[c]);
-    }
-  }
-  const float dw = half_bits_to_float((uint16_t)w.d);
-#pragma unroll
-  for (int c = 0; c < NCOLS; ++c) acc[c] = fmaf(dw, inner[c], acc[c]);
-}
-
 // ----------------------------------------------------------------- Q4_K ----
 // Registers of one lane for one Q4_K block half u: the 16-byte header (d,
 // dmin, 12 scale bytes) and qs[64u..64u+63] as 16 words, i.e. qs chunks
@@ -273,25 +131,6 @@ __device__ __forceinline__ void load_q4_gguf(const uint8_t* __restrict__ blk, in
     w.qs[4 * j + 2] = v.z;
     w.qs[4 * j + 3] = v.w;
   }
-}
-
-// Planar Q4_K tile in global memory (2304 bytes): lane L reads qs chunks
-// [512j + 16L] and its row's header at [2048 + 16i].
-__device__ __forceinline__ void load_q4_planar(const uint8_t* __restrict__ tile, int lane,
-                                               Q4Half& w) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 v = ldg_nc_v4(tile + 512 * j + 16 * lane);
-    w.qs[4 * j + 0] = v.x;
-    w.qs[4 * j + 1] = v.y;
-    w.qs[4 * j + 2] = v.z;
-    w.qs[4 * j + 3] = v.w;
-  }
-  const uint4 hv = ldg_nc_v4(tile + 2048 + 16 * (lane & 15));
-  w.hdr[0] = hv.x;
-  w.hdr[1] = hv.y;
-  w.hdr[2] = hv.z;
-  w.hdr[3] = hv.w;
 }
 
 // The same tile staged in shared memory.

@@ -30,16 +30,11 @@ namespace mmvq {
 template <int LAYOUT>
 __device__ __forceinline__ void rowgroup_range(const uint8_t* W, int64_t rows, int nb, int64_t rg,
                                                const uint8_t** p, int64_t* bytes) {
-  if (LAYOUT == kQ6Planar) {
-    *p = W + rg * nb * kTileBytes;
-    *bytes = (int64_t)nb * kTileBytes;
-  } else {
-    const int bb = (LAYOUT == kQ4Gguf) ? kQ4KBytes : kQ6KBytes;
-    const int64_t r0 = rg * kTileRows;
-    const int64_t r1 = min(r0 + kTileRows, rows);
-    *p = W + r0 * nb * bb;
-    *bytes = (r1 - r0) * nb * bb;
-  }
+  const int bb = (LAYOUT == kQ4Gguf) ? kQ4KBytes : kQ6KBytes;
+  const int64_t r0 = rg * kTileRows;
+  const int64_t r1 = min(r0 + kTileRows, rows);
+  *p = W + r0 * nb * bb;
+  *bytes = (r1 - r0) * nb * bb;
 }
 
 template <int LAYOUT, int NCOLS>

@@ -85,14 +85,12 @@ __global__ void __launch_bounds__(512) mmvq_grouped_kernel(
   const int nbq = K / kQK8;
   const int rb = act_row_bytes(K);
   const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
-  const int64_t expert_bytes =
-      LAYOUT == kQ4Planar ? n_rg * nb * kTileBytesQ4
-                          : rows * nb * (LAYOUT == kQ4Gguf ? kQ4KBytes : kQ6KBytes);
+  const int64_t expert_bytes = rows * nb * (LAYOUT == kQ4Gguf ? kQ4KBytes : kQ6KBytes);
 
   uint8_t* act = smem;
   float* da = reinterpret_cast<float*>(smem + kMaxCols * rb);
   float* sa = da + kMaxCols * nbq;
-  float* red = sa + ((LAYOUT == kQ4Gguf || LAYOUT == kQ4Planar) ? kMaxCols * nbq : 0);
+  float* red = sa + (LAYOUT == kQ4Gguf ? kMaxCols * nbq : 0);
   uint8_t* stage =
       reinterpret_cast<uint8_t*>(red + WK * kMaxCols * kTileRows) + (size_t)wk * 2 * kGgufStage;
 
@@ -146,7 +144,7 @@ __global__ void __launch_bounds__(512) mmvq_grouped_kernel(
         __syncthreads();
         // an invalid column is staged as zeros (d = 0, q = 0): its rows come out 0
         stage_q8_1(xq, K, n, [&](int c) { return cols_s[c]; }, act, da,
-                   (LAYOUT == kQ4Gguf || LAYOUT == kQ4Planar) ? sa : nullptr, tid, nthreads);
+                   LAYOUT == kQ4Gguf ? sa : nullptr, tid, nthreads);
         __syncthreads();
         staged_g = g;
         staged_p0 = p0;

@@ -61,18 +61,7 @@ __device__ __forceinline__ void rowgroup_dot(const uint8_t* __restrict__ W, int6
   const int i = lane & 15;
   const int h = lane >> 4;
   const int64_t row = rg * kTileRows + i;
-  if (LAYOUT == kQ6Planar) {
-    const uint8_t* tiles = W + (size_t)rg * nb * kTileBytes;
-    int b = wk;
-    Q6Half cur;
-    if (b < nb) load_q6_planar(tiles + (size_t)b * kTileBytes, lane, cur);
-    for (; b < nb; b += WK) {
-      Q6Half nxt;
-      if (b + WK < nb) load_q6_planar(tiles + (size_t)(b + WK) * kTileBytes, lane, nxt);
-      q6_dot<NC>(cur, h, b, act, rb, da, nbq, acc, srow, scs);
-      cur = nxt;
-    }
-  } else if (LAYOUT == kQ6Gguf) {
+  if (LAYOUT == kQ6Gguf) {
     const int64_t total_bytes = rows * nb * kQ6KBytes;
     const int64_t rr = min(row, rows - 1);
     int b = wk;
@@ -91,17 +80,6 @@ __device__ __forceinline__ void rowgroup_dot(const uint8_t* __restrict__ W, int6
       __syncwarp();
       q6_dot<NC>(cur, h, b, act, rb, da, nbq, acc, srow, scs);
       slot ^= 1;
-    }
-  } else if (LAYOUT == kQ4Planar) {
-    const uint8_t* tiles = W + (size_t)rg * nb * kTileBytesQ4;
-    int b = wk;
-    Q4Half cur;
-    if (b < nb) load_q4_planar(tiles + (size_t)b * kTileBytesQ4, lane, cur);
-    for (; b < nb; b += WK) {
-      Q4Half nxt;
-      if (b + WK < nb) load_q4_planar(tiles + (size_t)(b + WK) * kTileBytesQ4, lane, nxt);
-      q4_dot<NC>(cur, h, b, act, rb, da, sa, nbq, acc, srow, scs);
-      cur = nxt;
     }
   } else {
     const int64_t rr = min(row, rows - 1);
@@ -156,7 +134,7 @@ __device__ __forceinline__ void reduce_store(float (&acc)[NC], int lane, int wk,
 // Dynamic shared memory of a CTA with `nwarps` warps and `ncols` staged columns.
 __host__ __device__ inline size_t mmvq_smem_bytes(int layout, int K, int ncols, int nwarps) {
   size_t s = (size_t)ncols * act_row_bytes(K);                            // quants
-  s += (size_t)ncols * (K / kQK8) * 4 * ((layout == kQ4Gguf || layout == kQ4Planar) ? 2 : 1);
+  s += (size_t)ncols * (K / kQK8) * 4 * (layout == kQ4Gguf ? 2 : 1);
   s += (size_t)nwarps * kMaxCols * kTileRows * 4;                          // K-slice partials
   if (layout == kQ6Gguf) s += (size_t)nwarps * 2 * kGgufStage;             // cp.async ring
   return s;
