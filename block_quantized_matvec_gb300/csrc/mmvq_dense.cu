@@ -19,6 +19,7 @@
 // mid-size matrices are resident in one wave; large ones run persistently
 // and prefetch the next row group into L2 while computing the current one.
 #include <algorithm>
+#include <map>
 #include <mutex>
 #include <unordered_map>
 
@@ -135,13 +136,20 @@ int divisor_at_least(int nb, int want) {
 }
 
 // Raises a kernel's dynamic shared memory limit once it is first needed.
-int ensure_smem(const void* kern, size_t smem, size_t* smem_set, std::mutex* mu) {
-  std::lock_guard<std::mutex> lock(*mu);
-  if (smem > *smem_set) {
+// Raises the kernel's dynamic shared-memory limit on the current device to
+// at least `smem` (the attribute is per kernel and per device).
+int ensure_smem(const void* kern, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> set;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MMVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = set[{kern, dev}];
+  if (smem > have) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return MMVQ_ERR_CUDA;
-    *smem_set = smem;
+    have = smem;
   }
   return MMVQ_OK;
 }
@@ -160,7 +168,6 @@ template <int LAYOUT, int NCOLS>
 static int dense_config(int64_t rows, int K, DenseCfg* out) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, DenseCfg> cache;
-  static size_t smem_set = 0;  // the attribute is set before the first launch
   const uint64_t key = ((uint64_t)rows << 8) | (uint64_t)(K / kQK);
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -179,7 +186,7 @@ static int dense_config(int64_t rows, int K, DenseCfg* out) {
 
   auto occupancy = [&](int nwarps, size_t smem, int* per_sm) -> int {
     if (smem > limit) return MMVQ_ERR_SHAPE;
-    if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+    if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, 32 * nwarps, smem) !=
         cudaSuccess)
       return MMVQ_ERR_CUDA;

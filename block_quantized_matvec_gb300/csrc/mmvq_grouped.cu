@@ -19,7 +19,7 @@ namespace mmvq {
 int device_sms();
 size_t max_smem_optin();
 int divisor_at_least(int nb, int want);
-int ensure_smem(const void* kern, size_t smem, size_t* smem_set, std::mutex* mu);
+int ensure_smem(const void* kern, size_t smem);
 
 constexpr int kMaxGroups = 4096;
 
@@ -185,8 +185,7 @@ static int launch_grouped_t(const uint8_t* W, int n_experts, int64_t rows, int K
   }
   if (smem > limit) return MMVQ_ERR_SHAPE;
   static std::mutex mu;
-  static size_t smem_set = 0;  // the attribute is set before the first launch
-  if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+  if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * wk, smem) != cudaSuccess ||
       per_sm <= 0)

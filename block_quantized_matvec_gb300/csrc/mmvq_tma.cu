@@ -36,7 +36,7 @@ namespace mmvq {
 
 int device_sms();
 size_t max_smem_optin();
-int ensure_smem(const void* kern, size_t smem, size_t* smem_set, std::mutex* mu);
+int ensure_smem(const void* kern, size_t smem);
 
 __device__ unsigned int g_fault_word = 0;
 
@@ -655,7 +655,6 @@ template <int LAYOUT, int NCOLS>
 static int tma_config(int64_t rows, int K, TmaCfg* out) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, TmaCfg> cache;
-  static size_t smem_set = 0;  // the attribute is set before the first launch
   const uint64_t key = ((uint64_t)rows << 8) | (uint64_t)(K / kQK);
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -684,7 +683,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
     for (int G = 7; G >= 1 && best.G == 0; --G) {
       const size_t smem = tma_smem_bytes(LAYOUT, 2, K, NCOLS, G, 1);
       if (smem > limit) continue;
-      if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+      if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
       int per_sm = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (G + 1), smem) !=
           cudaSuccess)
@@ -709,7 +708,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
         }
       }
       if (S == 0) continue;
-      if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+      if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
       int per_sm = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (G * P + 1), smem) !=
           cudaSuccess)
@@ -831,7 +830,6 @@ template <int LAYOUT, int CM>
 static int grouped_config(int64_t rows, int K, int64_t est_active, GroupedCfg* out) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, GroupedCfg> cache;
-  static size_t smem_set = 0;  // the attribute is set before the first launch
   const uint64_t key = ((uint64_t)rows << 28) | ((uint64_t)(K / kQK) << 16) | (uint64_t)est_active;
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -868,7 +866,7 @@ static int grouped_config(int64_t rows, int K, int64_t est_active, GroupedCfg* o
   while (S > 2 && grouped_smem_bytes(LAYOUT, S, K, CM, G, P) > limit) --S;
   const size_t smem = grouped_smem_bytes(LAYOUT, S, K, CM, G, P);
   if (smem > limit) return MMVQ_ERR_SHAPE;
-  if (ensure_smem((const void*)kern, smem, &smem_set, &mu) != MMVQ_OK) return MMVQ_ERR_CUDA;
+  if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (G * P + 1), smem) !=
           cudaSuccess ||

@@ -17,6 +17,10 @@
  *    int32 arrays 4-byte aligned.
  *  - There is no CPU fallback: without a usable sm_103a device a launch
  *    fails with MMVQ_ERR_CUDA.
+ *  - Launch shapes are chosen on the first call for a shape and cached; the
+ *    caches are guarded, so calls may come from several host threads.  A
+ *    process may drive several GPUs of the same model (the cached shapes
+ *    assume one SM count); kernel attributes are set per device.
  *
  * Formats (the pages are the Strata engine's SYCL port: PRs #2746, #2340,
  * #2207, #1774 and issue #2801; the byte arrangement inside each block is
