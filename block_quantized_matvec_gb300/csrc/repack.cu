@@ -6,6 +6,8 @@
 // loads are aligned 16-byte loads; the draft head's subset is gathered from
 // the planar head).  Here the planes are kept per 16-row x 256-column tile
 // in the order the MMVQ warps read them (see include/mmvq.h).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace mmvq {
@@ -203,14 +205,17 @@ __global__ void __launch_bounds__(1024) route_groups_kernel(const int32_t* __res
   }
   if (lane == 31) wsum[warp] = x;
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int w = 0; w < 32; ++w) {
-      const int v = wsum[w];
-      wsum[w] = run;
-      run += v;
+  if (warp == 0) {  // exclusive scan of the warp totals, by shuffles
+    const int nw = (int)(blockDim.x >> 5);
+    const int v = lane < nw ? wsum[lane] : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
     }
-    wsum[32] = run;
+    if (lane < nw) wsum[lane] = inc - v;
+    if (lane == 31) wsum[32] = inc;
   }
   __syncthreads();
   int run = wsum[warp] + x - sum;
@@ -273,7 +278,9 @@ int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_
 int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
                         int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
                         cudaStream_t s) {
-  return launch_pdl(route_groups_kernel, dim3(1), dim3(1024), 0, s, topk, T * k, k, n_experts,
+  // each thread owns four experts; at least two warps
+  const int threads = std::max(64, std::min(1024, ((n_experts + 3) / 4 + 31) / 32 * 32));
+  return launch_pdl(route_groups_kernel, dim3(1), dim3(threads), 0, s, topk, T * k, k, n_experts,
                     expert_ids, offsets, act_index, slot_of, status);
 }
 
