@@ -454,8 +454,9 @@ def run_ours(args, rank, world, local_rank):
 
 def run_moe(args, rank, world, local_rank):
     """One step = the routed-expert hot path for T tokens: Q8_1 quantise the
-    hidden states, per-expert token lists from the top-k routing, grouped
-    gate|up MMVQ, SiLU(gate)*up requantised to Q8_1, grouped down MMVQ.
+    hidden states and build the per-expert token lists from the top-k routing
+    (one launch), grouped gate|up MMVQ, SiLU(gate)*up requantised to Q8_1,
+    grouped down MMVQ.
     Experts are planar Q4_K tiles; each step uses the next of 16 seeded
     routings, so consecutive steps read different experts.  Weight bytes =
     distinct experts read x (gate|up + down) bytes."""
@@ -497,18 +498,17 @@ def run_moe(args, rank, world, local_rank):
     def step(r, s=None, evs=None):
         rec = (lambda i: _record_external(evs[i], s)) if evs is not None else (lambda i: None)
         rec(0)
-        mmvq.quantize_q8_1(x_dev, out=xq)
+        # hidden-state Q8_1 and the per-expert lists in one launch
+        _, eids, offs, act, _, status = mmvq.quantize_route_groups(x_dev, topk_dev[r], E, xq=xq)
         rec(1)
-        eids, offs, act, _, status = mmvq.route_groups(topk_dev[r], E)
-        rec(2)
         mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_gu, E, 2 * F, H, eids, offs, act, xq, T, n, out=gu,
                      status=status)
-        rec(3)
+        rec(2)
         mmvq.silu_mul_quantize_q8_1(gu, F, out=hq)
-        rec(4)
+        rec(3)
         mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_dn, E, H, F, eids, offs, None, hq, n, n, out=y,
                      status=status)
-        rec(5)
+        rec(4)
 
     for r in range(R):
         step(r)
@@ -518,7 +518,7 @@ def run_moe(args, rank, world, local_rank):
     # between kernels, replayed after the timed region
     graphs, graphs_ev, events = [], [], []
     for r in range(R):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         for e in evs:
             e.record()
         torch.cuda.synchronize()
@@ -556,17 +556,17 @@ def run_moe(args, rank, world, local_rank):
             graphs_ev[r].replay()
             torch.cuda.synchronize()
             evs = events[r]
-            dur_runs.append([evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(5)])
+            dur_runs.append([evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(4)])
 
     distinct = [len(np.unique(t)) for t in topks]
     step_bytes = [metrics.moe_step_bytes(d, H, F) for d in distinct]
     total_bytes = sum(step_bytes[i % R] for i in range(args.steps))
-    names = ["quantize", "route", "grouped_gate_up", "silu_requant", "grouped_down"]
+    names = ["quantize_and_route", "grouped_gate_up", "silu_requant", "grouped_down"]
     mean_us = np.array(dur_runs).mean(axis=0)
     gu_bytes = np.mean([d * metrics.weight_bytes("q4_k", 2 * F, H) for d in distinct])
     dn_bytes = np.mean([d * metrics.weight_bytes("q4_k", H, F) for d in distinct])
     peak, peak_kind = load_peak()
-    achieved = gu_bytes / (mean_us[2] * 1e-6) / 1e9
+    achieved = gu_bytes / (mean_us[1] * 1e-6) / 1e9
     # DRAM bytes per gate|up launch: the profiled traffic / weight-byte ratio
     # (T=8 capture) applied to this run's mean weight bytes per launch
     ratio = profiled_field("mmvq_grouped_moe_t8.md", "traffic_over_weight_bytes_gate_up")
@@ -599,11 +599,11 @@ def run_moe(args, rank, world, local_rank):
         "e2e": {"value": round(np.mean(step_bytes) / e2e_s / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y.numel() * 4),
                 "steps": e2e_steps},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clk,
         "kernels_us": {nm: round(float(v), 3) for nm, v in zip(names, mean_us)},
-        "grouped_gbps": {"gate_up": round(gu_bytes / mean_us[2] / 1e3, 1),
-                         "down": round(dn_bytes / mean_us[4] / 1e3, 1)},
+        "grouped_gbps": {"gate_up": round(gu_bytes / mean_us[1] / 1e3, 1),
+                         "down": round(dn_bytes / mean_us[3] / 1e3, 1)},
     }
     return out
 

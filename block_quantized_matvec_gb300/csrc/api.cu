@@ -8,6 +8,10 @@
 namespace mmvq {
 int launch_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq, cudaStream_t s);
 int launch_silu_mul_quantize(const float* gu, int F, int n, void* xq, float* h_out, cudaStream_t s);
+int launch_quantize_route(const float* x, int K, int ncols, int64_t ldx, void* xq,
+                          const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                          int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
+                          int32_t* status, cudaStream_t stream);
 int launch_rmsnorm_quantize(const float* x, const float* w, float eps, int K, int ncols,
                             int64_t ldx, void* xq, float* y_out, cudaStream_t s);
 int launch_dense(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
@@ -63,6 +67,24 @@ int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq,
   if (K <= 0 || K % mmvq::kQK8 != 0 || ldx < K || ncols < 1 || ncols > 65535) return MMVQ_ERR_SHAPE;
   if (!aligned(x, 4) || !aligned(xq, 16)) return MMVQ_ERR_ALIGN;
   return mmvq::launch_quantize_q8_1(x, K, ncols, ldx, xq, (cudaStream_t)stream);
+}
+
+int mmvq_quantize_route_groups(const float* x, int K, int ncols, int64_t ldx, void* xq,
+                               const int32_t* topk, int T, int k, int n_experts,
+                               int32_t* expert_ids, int32_t* token_offsets, int32_t* act_index,
+                               int32_t* slot_of, int32_t* status, mmvq_stream_t stream) {
+  if (!x || !xq || !expert_ids || !token_offsets || !act_index || !slot_of) return MMVQ_ERR_NULL;
+  if (T > 0 && !topk) return MMVQ_ERR_NULL;
+  if (K <= 0 || K % mmvq::kQK8 != 0 || ldx < K || ncols < 1 || ncols > 65535) return MMVQ_ERR_SHAPE;
+  if (n_experts < 1 || n_experts > 4096 || T < 0 || k < 1 || (int64_t)T * k > 65536)
+    return MMVQ_ERR_SHAPE;
+  if (!aligned(x, 4) || !aligned(xq, 16) || (topk && !aligned(topk, 4)) ||
+      !aligned(expert_ids, 4) || !aligned(token_offsets, 4) || !aligned(act_index, 4) ||
+      !aligned(slot_of, 4) || (status && !aligned(status, 4)))
+    return MMVQ_ERR_ALIGN;
+  return mmvq::launch_quantize_route(x, K, ncols, ldx, xq, topk, T, k, n_experts, expert_ids,
+                                     token_offsets, act_index, slot_of, status,
+                                     (cudaStream_t)stream);
 }
 
 static bool dense_type(int type) {

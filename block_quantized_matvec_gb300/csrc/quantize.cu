@@ -6,6 +6,7 @@
 // per block, one value per lane; IEEE division and roundf (no fast-math),
 // so the bytes are exactly those of the plain definition.
 #include "common.cuh"
+#include "route.cuh"
 
 namespace mmvq {
 
@@ -160,6 +161,38 @@ int launch_rmsnorm_quantize(const float* x, const float* w, float eps, int K, in
                     K, ldx, static_cast<uint8_t*>(xq), y_out);
 }
 
+// The first step of an expert layer in one launch: blocks 0 .. n-2 quantise
+// the hidden states as quantize_q8_1_kernel, the last block builds the
+// per-expert token lists as route_groups_kernel (the two are independent).
+// Writes activations, so no early start of the next kernel.
+__global__ void __launch_bounds__(256) quantize_route_kernel(
+    const float* __restrict__ x, int K, int ncols, int64_t ldx, uint8_t* __restrict__ xq,
+    const int32_t* __restrict__ topk, int n_slots, int k, int n_experts,
+    int32_t* __restrict__ expert_ids, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ act_index, int32_t* __restrict__ slot_of, int32_t* __restrict__ status) {
+  grid_dependency_wait();
+  if (blockIdx.x == gridDim.x - 1) {
+    route_groups_cta(topk, n_slots, k, n_experts, expert_ids, offsets, act_index, slot_of, status);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int nbq = K / kQK8;
+  const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (blk >= (int64_t)ncols * nbq) return;
+  const int c = (int)(blk / nbq);
+  const int kb = (int)(blk - (int64_t)c * nbq);
+  quantize_lane(x[(int64_t)c * ldx + kb * kQK8 + lane], xq + blk * kQ81Bytes, lane);
+}
+
+int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                        int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
+                        int32_t* status, cudaStream_t s);
+
+int launch_quantize_route(const float* x, int K, int ncols, int64_t ldx, void* xq,
+                          const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                          int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
+                          int32_t* status, cudaStream_t stream);
+
 int launch_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq,
                          cudaStream_t stream) {
   const int64_t blocks = (int64_t)ncols * (K / kQK8);
@@ -174,6 +207,25 @@ int launch_silu_mul_quantize(const float* gu, int F, int n, void* xq, float* h_o
   const int grid = (int)((blocks + 7) / 8);
   return launch_pdl(silu_mul_quantize_kernel, dim3(grid), dim3(256), 0, stream, gu, F, n,
                     static_cast<uint8_t*>(xq), h_out);
+}
+
+// One launch when the routing fits one 256-thread block (four experts per
+// thread), else the two kernels back to back.
+int launch_quantize_route(const float* x, int K, int ncols, int64_t ldx, void* xq,
+                          const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
+                          int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
+                          int32_t* status, cudaStream_t stream) {
+  if (n_experts > 4 * 256) {
+    const int rc = launch_quantize_q8_1(x, K, ncols, ldx, xq, stream);
+    if (rc != MMVQ_OK) return rc;
+    return launch_route_groups(topk, T, k, n_experts, expert_ids, token_offsets, act_index,
+                               slot_of, status, stream);
+  }
+  const int64_t blocks = (int64_t)ncols * (K / kQK8);
+  const int grid = (int)((blocks + 7) / 8) + 1;
+  return launch_pdl(quantize_route_kernel, dim3(grid), dim3(256), 0, stream, x, K, ncols, ldx,
+                    static_cast<uint8_t*>(xq), topk, T * k, k, n_experts, expert_ids,
+                    token_offsets, act_index, slot_of, status);
 }
 
 }  // namespace mmvq

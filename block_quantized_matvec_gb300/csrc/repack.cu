@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "route.cuh"
 
 namespace mmvq {
 
@@ -162,8 +163,8 @@ __global__ void __launch_bounds__(256) gather_planar_kernel(const uint8_t* __res
   *reinterpret_cast<uint4*>(out + t * kTileBytes + 16 * q) = *reinterpret_cast<const uint4*>(buf);
 }
 
-// Per-expert token lists (one CTA of 1024 threads): counting sort of the
-// routing slots by expert, stable in slot order.  Slot s = t*k + j.
+// Per-expert token lists, one CTA (route_groups_cta); the next kernel may
+// start at once (it waits for this one before it reads the lists).
 __global__ void __launch_bounds__(1024) route_groups_kernel(const int32_t* __restrict__ topk,
                                                             int n_slots, int k, int n_experts,
                                                             int32_t* __restrict__ expert_ids,
@@ -171,87 +172,9 @@ __global__ void __launch_bounds__(1024) route_groups_kernel(const int32_t* __res
                                                             int32_t* __restrict__ act_index,
                                                             int32_t* __restrict__ slot_of,
                                                             int32_t* __restrict__ status) {
-  __shared__ int cnt[4096];
-  __shared__ int wsum[33];
-  const int tid = threadIdx.x;
   grid_launch_dependents();
   grid_dependency_wait();
-  for (int e = tid; e < n_experts; e += blockDim.x) cnt[e] = 0;
-  __syncthreads();
-  for (int s = tid; s < n_slots; s += blockDim.x) {
-    const int e = topk[s];
-    if (e >= 0 && e < n_experts) {
-      atomicAdd(&cnt[e], 1);
-    } else if (status) {
-      *status = MMVQ_ERR_ROUTING;
-    }
-  }
-  __syncthreads();
-  // exclusive scan: thread tid owns experts [4tid, 4tid+4)
-  int local[4];
-  int sum = 0;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = 4 * tid + u;
-    local[u] = e < n_experts ? cnt[e] : 0;
-    sum += local[u];
-  }
-  const int lane = tid & 31, warp = tid >> 5;
-  int x = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += v;
-  }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  if (warp == 0) {  // exclusive scan of the warp totals, by shuffles
-    const int nw = (int)(blockDim.x >> 5);
-    const int v = lane < nw ? wsum[lane] : 0;
-    int inc = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += t;
-    }
-    if (lane < nw) wsum[lane] = inc - v;
-    if (lane == 31) wsum[32] = inc;
-  }
-  __syncthreads();
-  int run = wsum[warp] + x - sum;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = 4 * tid + u;
-    if (e < n_experts) {
-      offsets[e] = run;
-      expert_ids[e] = e;
-      cnt[e] = run;  // becomes the placement cursor
-    }
-    run += local[u];
-  }
-  if (tid == 0) offsets[n_experts] = wsum[32];
-  __syncthreads();
-  // stable placement by one warp, 32 slots at a time in slot order
-  if (warp == 0) {
-    for (int base = 0; base < n_slots; base += 32) {
-      const int s = base + lane;
-      int e = -1;
-      if (s < n_slots) {
-        const int v = topk[s];
-        if (v >= 0 && v < n_experts) e = v;
-      }
-      const unsigned same = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(same & ((1u << lane) - 1u));
-      if (e >= 0) {
-        const int p = cnt[e] + rank;
-        act_index[p] = s / k;
-        slot_of[p] = s;
-      }
-      __syncwarp();
-      if (e >= 0 && rank == 0) cnt[e] += __popc(same);
-      __syncwarp();
-    }
-  }
+  route_groups_cta(topk, n_slots, k, n_experts, expert_ids, offsets, act_index, slot_of, status);
 }
 
 int launch_repack_planar(int type, const void* W, int64_t rows, int K, void* P, cudaStream_t s) {

@@ -39,6 +39,7 @@ SIGNATURES = {
     "mmvq_debug_block_sums": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P, _P]),
     "mmvq_grouped": (_I, [_I, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P]),
     "mmvq_route_groups": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "mmvq_quantize_route_groups": (_I, [_P, _I, _I, _I64, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "mmvq_silu_mul_quantize_q8_1": (_I, [_P, _I, _I, _P, _P, _P]),
     "mmvq_planar_bytes": (_I64, [_I, _I64, _I]),
     "mmvq_repack_planar": (_I, [_I, _P, _I64, _I, _P, _P]),
@@ -164,6 +165,32 @@ def grouped(type_: int, W_experts: torch.Tensor, n_experts: int, rows: int, K: i
                               _ptr(offsets), expert_ids.numel(), _ptr(act_index), _ptr(xq),
                               n_xq_cols, _ptr(out), _ptr(status), _stream(stream)), "mmvq_grouped")
     return out
+
+
+def quantize_route_groups(x: torch.Tensor, topk: torch.Tensor, n_experts: int,
+                          xq: torch.Tensor | None = None, stream=None):
+    """One launch: Q8_1 of x [ncols, K] and the per-expert lists of topk [T, k]
+    -> (xq, expert_ids, offsets, act_index, slot_of, status)."""
+    _dev(x, "x")
+    _dev(topk, "topk")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    ncols, K = x.shape
+    T, k = topk.shape
+    dev = x.device
+    if xq is None:
+        xq = torch.empty((ncols, K // 32, Q8_1_BYTES), dtype=torch.uint8, device=dev)
+    eids = torch.empty(n_experts, dtype=torch.int32, device=dev)
+    offs = torch.empty(n_experts + 1, dtype=torch.int32, device=dev)
+    act = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    slot = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().mmvq_quantize_route_groups(_ptr(x), K, ncols, K, _ptr(xq),
+                                            _ptr(topk) if T else None, T, k, n_experts,
+                                            _ptr(eids), _ptr(offs), _ptr(act), _ptr(slot),
+                                            _ptr(status), _stream(stream)),
+           "mmvq_quantize_route_groups")
+    return xq, eids, offs, act, slot, status
 
 
 def route_groups(topk: torch.Tensor, n_experts: int, stream=None):

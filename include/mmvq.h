@@ -195,6 +195,20 @@ MMVQ_API int mmvq_route_groups(const int32_t* topk, int T, int k, int n_experts,
                       int32_t* status, mmvq_stream_t stream);
 
 /*
+ * The first step of an expert layer in one launch: mmvq_quantize_q8_1 of the
+ * hidden states x and mmvq_route_groups of topk (the two are independent;
+ * every output is the same bits as the two calls give).  Arguments and
+ * limits are those of the two calls.  With n_experts > 1024 it issues the two
+ * kernels one after the other.  No counterpart on the pages (their engine
+ * launches them separately).
+ */
+MMVQ_API int mmvq_quantize_route_groups(const float* x, int K, int ncols, int64_t ldx, void* xq,
+                                        const int32_t* topk, int T, int k, int n_experts,
+                                        int32_t* expert_ids, int32_t* token_offsets,
+                                        int32_t* act_index, int32_t* slot_of, int32_t* status,
+                                        mmvq_stream_t stream);
+
+/*
  * SiLU(gate) * up, requantised to Q8_1 between the grouped gate/up and down
  * calls.  gu: fp32 [n][2F] rows laid out [gate F | up F] (the grouped
  * gate/up output when the expert's first F rows are gate and the next F

@@ -99,6 +99,11 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_rmsnorm_quantize_q8_1(*r[:2], -1.0, *r[3:]) == mmvq.ERR_SHAPE
     assert L.mmvq_rmsnorm_quantize_q8_1(*r[:2], float("nan"), *r[3:]) == mmvq.ERR_SHAPE
     assert L.mmvq_rmsnorm_quantize_q8_1(*r[:6], A + 4, *r[7:]) == mmvq.ERR_ALIGN
+    qr = (A, 2560, 1, 2560, A, A, 1, 8, 256, A, A, A, A, None, None)
+    assert L.mmvq_quantize_route_groups(*qr[:5], None, *qr[6:]) == mmvq.ERR_NULL      # topk, T > 0
+    assert L.mmvq_quantize_route_groups(*qr[:1], 2560 + 16, *qr[2:]) == mmvq.ERR_SHAPE
+    assert L.mmvq_quantize_route_groups(*qr[:8], 4097, *qr[9:]) == mmvq.ERR_SHAPE
+    assert L.mmvq_quantize_route_groups(*qr[:4], A + 4, *qr[5:]) == mmvq.ERR_ALIGN
     assert L.mmvq_selftest_wait_timeout(0, None) == mmvq.ERR_SHAPE
     assert L.mmvq_selftest_wait_timeout(100001, None) == mmvq.ERR_SHAPE
     assert L.mmvq_route_groups(A, 4, 8, 0, A, A, A, A, None, None) == mmvq.ERR_SHAPE

@@ -178,3 +178,16 @@ def test_grouped_planar_is_bitwise_repeatable(kind):
     outs = [host(mmvq.grouped(_KIND_TYPE[kind], W, E, rows, K, g_eids, g_offs, g_act, xqd, T,
                               T * k)) for _ in range(3)]
     assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
+
+
+@pytest.mark.parametrize("T,k,E,K", [(1, 8, 256, 2560), (8, 8, 256, 2560), (3, 2, 1024, 768),
+                                     (4, 8, 2048, 256), (5, 3, 7, 512)])
+def test_quantize_route_in_one_launch_matches_the_two_calls(T, k, E, K):
+    topk = dev(synth.routing(T, k, E, salt=E + T))
+    x = dev(synth.activations(K, T, salt=E + T))
+    xq, eids, offs, act, slot, status = mmvq.quantize_route_groups(x, topk, E)
+    r_eids, r_offs, r_act, r_slot, r_status = mmvq.route_groups(topk, E)
+    assert np.array_equal(host(xq), host(mmvq.quantize_q8_1(x)))
+    assert np.array_equal(host(xq), oracle.quantize_q8_1(host(x)))
+    for a, b in ((eids, r_eids), (offs, r_offs), (act, r_act), (slot, r_slot), (status, r_status)):
+        assert np.array_equal(host(a), host(b))
