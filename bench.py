@@ -118,6 +118,24 @@ def profiled_traffic(summary: str):
     return None if v is None else int(v)
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the slowest replica sets the job's
+    time); the value itself with one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
 def load_peak():
     p = os.path.join(HERE, "MEASURED_PEAKS.json")
     try:
@@ -331,8 +349,7 @@ def run_ours(args, rank, world, local_rank):
         graph.replay()
     torch.cuda.synchronize()
     clocks.wait_first_sample()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -343,12 +360,8 @@ def run_ours(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-        dist.barrier()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    barrier(world)
 
     # per-case durations from the event nodes of the last step
     q_us = np.array([evs[3 * ci].elapsed_time(evs[3 * ci + 1]) * 1e3 for ci in range(len(case_list))])
@@ -407,11 +420,7 @@ def run_ours(args, rank, world, local_rank):
         graph.replay()
         y_pinned.copy_(y_dev, non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - w0) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks((time.perf_counter() - w0) / e2e_steps, world, dev)
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -541,6 +550,7 @@ def run_moe(args, rank, world, local_rank):
     clocks.wait_first_sample()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
     clocks.mark()
     t0.record(stream)
     for i in range(args.steps):
@@ -548,7 +558,8 @@ def run_moe(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    barrier(world)
 
     dur_runs = []
     for rep in range(4):
@@ -580,15 +591,17 @@ def run_moe(args, rank, world, local_rank):
         graphs[i % R].replay()
         y_pinned.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - w0) / e2e_steps
+    e2e_s = max_over_ranks((time.perf_counter() - w0) / e2e_steps, world, dev)
 
     out = {
-        "metric": METRIC, "value": round(total_bytes / (elapsed_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+        "metric": METRIC, "value": round(world * total_bytes / (elapsed_ms * 1e-3) / 1e9, 1),
+        "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a + fp32",
         "data": "synthetic (seeded generators shaped like the pages' matrices)",
         "config": {"workload": WORKLOAD_DESC[args.workload], "tokens": T, "routings": R,
+                   "parallelism": f"replicas x{world}",
                    "distinct_experts_mean": float(np.mean(distinct)),
                    "timing": "CUDA graph replay of whole steps; per-kernel times from a "
                              "second graph with event nodes between the five kernels"},
@@ -596,7 +609,7 @@ def run_moe(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 3), "traffic": gu_traffic,
                      "algorithmic_bytes_per_launch": round(gu_bytes),
                      "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "grouped gate|up MMVQ"},
-        "e2e": {"value": round(np.mean(step_bytes) / e2e_s / 1e9, 1), "unit": UNIT,
+        "e2e": {"value": round(world * np.mean(step_bytes) / e2e_s / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y.numel() * 4),
                 "steps": e2e_steps},
         "gpu_launches": 4 * args.steps,
