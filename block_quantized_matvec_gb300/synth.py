@@ -78,6 +78,21 @@ def q4_k_weights(rows: int, K: int, salt: int = 0, seed: int = SEED_WEIGHTS) -> 
     return w.reshape(rows, nb, Q4_K_BLOCK_BYTES)
 
 
+def q5_k_weights(rows: int, K: int, salt: int = 0, seed: int = SEED_WEIGHTS) -> np.ndarray:
+    """Q5_K weight matrix as GGUF-ordered blocks, shape ``[rows, K//256, 176]`` uint8:
+    fp16 d and dmin uniform in [1e-3, 1e-2], every other byte (scales, qh, qs) uniform."""
+    if K % QK_K:
+        raise ValueError("K must be a multiple of 256")
+    nb = K // QK_K
+    n = rows * nb
+    rng = _rng(seed, 5000 + salt)
+    w = np.empty((n, 176), dtype=np.uint8)
+    w[:, 0:2] = _fp16_uniform(rng, n, 1e-3, 1e-2)                            # d
+    w[:, 2:4] = _fp16_uniform(rng, n, 1e-3, 1e-2)                            # dmin
+    w[:, 4:176] = rng.integers(0, 256, size=(n, 172), dtype=np.uint8)        # scales | qh | qs
+    return w.reshape(rows, nb, 176)
+
+
 def expert_weights(kind: str, n_experts: int, rows: int, K: int, salt: int = 0,
                    seed: int = SEED_WEIGHTS) -> np.ndarray:
     """Stacked per-expert matrices ``[n_experts, rows, K//256, block]``."""

@@ -25,12 +25,14 @@ _lock = threading.Lock()
 _lib = None
 
 TYPE_Q4_K = 12
+TYPE_Q5_K = 13
 TYPE_Q6_K = 14
 TYPE_Q6_K_PLANAR = 1014
 TYPE_Q4_K_PLANAR = 1012
+TYPE_Q5_K_PLANAR = 1013
 
 Q81_BYTES = 36
-BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210}
+BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q5_K: 176, TYPE_Q6_K: 210}
 
 
 def build(force: bool = False) -> str:
@@ -62,6 +64,11 @@ def _load():
             lib.orc_planar_bytes.restype = I64
             lib.orc_planar_bytes_q4.argtypes = [I64, I]
             lib.orc_planar_bytes_q4.restype = I64
+            lib.orc_planar_bytes_q5.argtypes = [I64, I]
+            lib.orc_planar_bytes_q5.restype = I64
+            lib.orc_repack_planar_q5.argtypes = [P, I64, I, P]
+            lib.orc_unpack_planar_q5.argtypes = [P, I64, I, P]
+            lib.orc_decode_q5_k.argtypes = [P, P, P, P, P, P]
             lib.orc_repack_planar_q4.argtypes = [P, I64, I, P]
             lib.orc_unpack_planar_q4.argtypes = [P, I64, I, P]
             lib.orc_repack_planar.argtypes = [P, I64, I, P]
@@ -125,6 +132,18 @@ def decode_q6_k(block: np.ndarray):
     return q, sc, float(d[0])
 
 
+def decode_q5_k(block: np.ndarray):
+    b = np.ascontiguousarray(block, dtype=np.uint8)
+    assert b.size == 176
+    q = np.empty(256, np.uint8)
+    sc = np.empty(8, np.uint8)
+    m = np.empty(8, np.uint8)
+    d = np.empty(1, np.float32)
+    dmin = np.empty(1, np.float32)
+    _load().orc_decode_q5_k(_p(b), _p(q), _p(sc), _p(m), _p(d), _p(dmin))
+    return q, sc, m, float(d[0]), float(dmin[0])
+
+
 def decode_q4_k(block: np.ndarray):
     b = np.ascontiguousarray(block, dtype=np.uint8)
     assert b.size == 144
@@ -137,27 +156,31 @@ def decode_q4_k(block: np.ndarray):
     return q, sc, m, float(d[0]), float(dmin[0])
 
 
-def planar_bytes(rows: int, K: int, type_: int = TYPE_Q6_K) -> int:
+def _planar_fns(type_: int):
+    lib = _load()
     if type_ == TYPE_Q4_K:
-        return int(_load().orc_planar_bytes_q4(rows, K))
-    return int(_load().orc_planar_bytes(rows, K))
+        return lib.orc_planar_bytes_q4, lib.orc_repack_planar_q4, lib.orc_unpack_planar_q4
+    if type_ == TYPE_Q5_K:
+        return lib.orc_planar_bytes_q5, lib.orc_repack_planar_q5, lib.orc_unpack_planar_q5
+    return lib.orc_planar_bytes, lib.orc_repack_planar, lib.orc_unpack_planar
+
+
+def planar_bytes(rows: int, K: int, type_: int = TYPE_Q6_K) -> int:
+    return int(_planar_fns(type_)[0](rows, K))
 
 
 def repack_planar(W: np.ndarray, rows: int, K: int, type_: int = TYPE_Q6_K) -> np.ndarray:
-    """GGUF blocks of type_ (Q6_K or Q4_K) -> planar tiles."""
+    """GGUF blocks of type_ (Q6_K, Q5_K or Q4_K) -> planar tiles."""
     W = np.ascontiguousarray(W, dtype=np.uint8)
     out = np.empty(planar_bytes(rows, K, type_), dtype=np.uint8)
-    fn = _load().orc_repack_planar_q4 if type_ == TYPE_Q4_K else _load().orc_repack_planar
-    _check(fn(_p(W), rows, K, _p(out)), "repack_planar")
+    _check(_planar_fns(type_)[1](_p(W), rows, K, _p(out)), "repack_planar")
     return out
 
 
 def unpack_planar(P: np.ndarray, rows: int, K: int, type_: int = TYPE_Q6_K) -> np.ndarray:
     P = np.ascontiguousarray(P, dtype=np.uint8)
-    bb = 144 if type_ == TYPE_Q4_K else 210
-    out = np.empty((rows, K // 256, bb), dtype=np.uint8)
-    fn = _load().orc_unpack_planar_q4 if type_ == TYPE_Q4_K else _load().orc_unpack_planar
-    _check(fn(_p(P), rows, K, _p(out)), "unpack_planar")
+    out = np.empty((rows, K // 256, BLOCK_BYTES[type_]), dtype=np.uint8)
+    _check(_planar_fns(type_)[2](_p(P), rows, K, _p(out)), "unpack_planar")
     return out
 
 

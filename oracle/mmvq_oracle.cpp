@@ -20,6 +20,12 @@
 //    6-bit scales/mins for 8 sub-blocks of 32, qs[128] nibbles; value
 //    d*sc*q - dmin*m (GGUF Q4_K arrangement).  The min term reaches the dot
 //    product through the Q8_1 sum s.
+//  * Q5_K weights (176 B per 256): the pages run Q5_K matrices through the
+//    same wide kernels (PR #2340 "ld_i4_a4"; the A770 dense_bench table)
+//    without giving the block; read as the GGUF Q5_K arrangement: fp16 d,
+//    fp16 dmin, the Q4_K scale/min bytes, qh[32] (bit j of qh[l] is the
+//    fifth bit of weight l of sub-block j) and qs[128] as in Q4_K; code
+//    q in 0..31, value d*sc*q - dmin*m.
 //  * Per-32-block integer sums (int8 dot products, PR #2746 "INT8 DP4A
 //    operations, scales, FP32 accumulation"), the FP32 block term
 //    d_w*d_a*sumi (minus dmin*m*s_a for Q4_K), and the FP32 sum over blocks
@@ -60,6 +66,10 @@ const int kQ6KBytes = 210;  // ql[128] qh[64] scales[16] d
 const int kQ4KBytes = 144;  // d dmin scales[12] qs[128]
 
 const int kTypeQ4K = 12;
+const int kTypeQ5K = 13;
+const int kQ5KBytes = 176;  // d dmin scales[12] qh[32] qs[128]
+const int kTypeQ5KPlanar = 1013;
+const int kTileBytesQ5 = 2816;  // 16 x 176
 const int kTypeQ6K = 14;
 const int kTypeQ6KPlanar = 1014;
 const int kTypeQ4KPlanar = 1012;
@@ -198,11 +208,7 @@ void decode_q6_k(const uint8_t* blk, uint8_t q[kQK], int8_t sc[16], float* d) {
 // qs chunk c (32 bytes qs[32c..32c+31]): low nibbles are sub-block 2c, high
 // nibbles sub-block 2c+1.  Value = d*sc*q - dmin*m.
 
-void decode_q4_k(const uint8_t* blk, uint8_t q[kQK], uint8_t sc[8], uint8_t m[8], float* d,
-                 float* dmin) {
-  *d = f16_to_f32(rd16(blk + 0));
-  *dmin = f16_to_f32(rd16(blk + 2));
-  const uint8_t* s = blk + 4;
+void unpack_scales_mins(const uint8_t* s, uint8_t sc[8], uint8_t m[8]) {
   for (int j = 0; j < 8; ++j) {
     if (j < 4) {
       sc[j] = s[j] & 63;
@@ -212,11 +218,39 @@ void decode_q4_k(const uint8_t* blk, uint8_t q[kQK], uint8_t sc[8], uint8_t m[8]
       m[j] = (uint8_t)((s[j + 4] >> 4) | ((s[j] >> 6) << 4));
     }
   }
+}
+
+void decode_q4_k(const uint8_t* blk, uint8_t q[kQK], uint8_t sc[8], uint8_t m[8], float* d,
+                 float* dmin) {
+  *d = f16_to_f32(rd16(blk + 0));
+  *dmin = f16_to_f32(rd16(blk + 2));
+  unpack_scales_mins(blk + 4, sc, m);
   const uint8_t* qs = blk + 16;
   for (int c = 0; c < 4; ++c) {
     for (int l = 0; l < 32; ++l) {
       q[64 * c + l] = qs[32 * c + l] & 0xf;
       q[64 * c + 32 + l] = qs[32 * c + l] >> 4;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- Q5_K ----
+// GGUF Q5_K: d | dmin | scales[12] (as Q4_K) | qh[32] | qs[128].  Sub-block j
+// (weights 32j .. 32j+31) takes its low 4 bits from qs chunk j/2 (low nibble
+// for even j, high for odd j) and, for weight l of the sub-block, its fifth
+// bit from bit j of qh[l].  Value = d*sc*q - dmin*m, q in 0..31.
+void decode_q5_k(const uint8_t* blk, uint8_t q[kQK], uint8_t sc[8], uint8_t m[8], float* d,
+                 float* dmin) {
+  *d = f16_to_f32(rd16(blk + 0));
+  *dmin = f16_to_f32(rd16(blk + 2));
+  unpack_scales_mins(blk + 4, sc, m);
+  const uint8_t* qh = blk + 16;
+  const uint8_t* qs = blk + 48;
+  for (int j = 0; j < 8; ++j) {
+    for (int l = 0; l < 32; ++l) {
+      const int lo = (qs[32 * (j / 2) + l] >> (4 * (j % 2))) & 0xf;
+      const int hi = (qh[l] >> j) & 1;
+      q[32 * j + l] = (uint8_t)(lo | (hi << 4));
     }
   }
 }
@@ -266,6 +300,40 @@ void unpack_planar_q4(const uint8_t* P, int64_t rows, int K, uint8_t* W) {
                        W + (r * nb + b) * kQ4KBytes);
 }
 
+// Planar Q5_K tile T(g, b), 2816 bytes, lane L = 16u + i (u = half of the
+// block: sub-blocks 4u..4u+3):
+//   [512j + 16L, +16),  j=0..3 : qs[64u + 16j .. +15]
+//   [2048 + 16i, +16)           : the 16-byte header (d, dmin, scales[12])
+//   [2304 + 32i, +32)           : qh[0..31] (both halves read all of it)
+int64_t planar_bytes_q5(int64_t rows, int K) {
+  const int64_t groups = (rows + kTileRows - 1) / kTileRows;
+  return groups * (int64_t)(K / kQK) * kTileBytesQ5;
+}
+
+void block_to_tile_q5(const uint8_t* blk, int i, uint8_t* tile) {
+  for (int u = 0; u < 2; ++u)
+    for (int j = 0; j < 4; ++j)
+      std::memcpy(tile + 512 * j + 16 * (16 * u + i), blk + 48 + 64 * u + 16 * j, 16);
+  std::memcpy(tile + 2048 + 16 * i, blk, 16);
+  std::memcpy(tile + 2304 + 32 * i, blk + 16, 32);
+}
+
+void tile_to_block_q5(const uint8_t* tile, int i, uint8_t* blk) {
+  for (int u = 0; u < 2; ++u)
+    for (int j = 0; j < 4; ++j)
+      std::memcpy(blk + 48 + 64 * u + 16 * j, tile + 512 * j + 16 * (16 * u + i), 16);
+  std::memcpy(blk, tile + 2048 + 16 * i, 16);
+  std::memcpy(blk + 16, tile + 2304 + 32 * i, 32);
+}
+
+void unpack_planar_q5(const uint8_t* P, int64_t rows, int K, uint8_t* W) {
+  const int nb = K / kQK;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int b = 0; b < nb; ++b)
+      tile_to_block_q5(P + ((r / kTileRows) * nb + b) * kTileBytesQ5, (int)(r % kTileRows),
+                       W + (r * nb + b) * kQ5KBytes);
+}
+
 // Copies one GGUF block (row i of tile) into / out of its tile slots.
 void block_to_tile(const uint8_t* blk, int i, uint8_t* tile) {
   for (int h = 0; h < 2; ++h) {
@@ -294,6 +362,7 @@ void tile_to_block(const uint8_t* tile, int i, uint8_t* blk) {
 int block_bytes(int type) {
   if (type == kTypeQ6K) return kQ6KBytes;
   if (type == kTypeQ4K) return kQ4KBytes;
+  if (type == kTypeQ5K) return kQ5KBytes;
   return 0;
 }
 
@@ -337,10 +406,13 @@ void block_terms(int type, const uint8_t* blk, const uint8_t* xq, int nbq, int c
       t_out[j] = t;
       abs_out[j] = std::fabs(t);
     }
-  } else {
+  } else {  // Q4_K and Q5_K: codes without offset, scale and min per 32
     uint8_t q[kQK], sc[8], m[8];
     float d, dmin;
-    decode_q4_k(blk, q, sc, m, &d, &dmin);
+    if (type == kTypeQ5K)
+      decode_q5_k(blk, q, sc, m, &d, &dmin);
+    else
+      decode_q4_k(blk, q, sc, m, &d, &dmin);
     for (int j = 0; j < 8; ++j) {
       const Q81 a = q81_at(xq, nbq, col, 8 * b + j);
       int32_t acc = 0;
@@ -434,6 +506,29 @@ void orc_decode_q4_k(const uint8_t* blk, uint8_t* q256, uint8_t* sc8, uint8_t* m
 
 int64_t orc_planar_bytes(int64_t rows, int K) { return planar_bytes(rows, K); }
 int64_t orc_planar_bytes_q4(int64_t rows, int K) { return planar_bytes_q4(rows, K); }
+int64_t orc_planar_bytes_q5(int64_t rows, int K) { return planar_bytes_q5(rows, K); }
+
+void orc_decode_q5_k(const uint8_t* blk, uint8_t* q256, uint8_t* sc8, uint8_t* m8, float* d,
+                     float* dmin) {
+  decode_q5_k(blk, q256, sc8, m8, d, dmin);
+}
+
+int orc_repack_planar_q5(const uint8_t* W, int64_t rows, int K, uint8_t* P) {
+  if (rows <= 0 || K <= 0 || K % kQK != 0) return -2;
+  const int nb = K / kQK;
+  std::memset(P, 0, (size_t)planar_bytes_q5(rows, K));
+  for (int64_t r = 0; r < rows; ++r)
+    for (int b = 0; b < nb; ++b)
+      block_to_tile_q5(W + (r * nb + b) * kQ5KBytes, (int)(r % kTileRows),
+                       P + ((r / kTileRows) * nb + b) * kTileBytesQ5);
+  return 0;
+}
+
+int orc_unpack_planar_q5(const uint8_t* P, int64_t rows, int K, uint8_t* W) {
+  if (rows <= 0 || K <= 0 || K % kQK != 0) return -2;
+  unpack_planar_q5(P, rows, K, W);
+  return 0;
+}
 
 int orc_repack_planar_q4(const uint8_t* W, int64_t rows, int K, uint8_t* P) {
   if (rows <= 0 || K <= 0 || K % kQK != 0) return -2;
@@ -493,8 +588,14 @@ int orc_gather_planar_rows(const uint8_t* P, int64_t rows, int K, const int32_t*
 int orc_gemv(int type, const uint8_t* W, int64_t rows, int K, const uint8_t* xq, int ncols,
              float* y, float* bound) {
   if (rows <= 0 || K <= 0 || K % kQK != 0 || ncols < 1) return -2;
-  if (type == kTypeQ6K || type == kTypeQ4K) {
+  if (type == kTypeQ6K || type == kTypeQ4K || type == kTypeQ5K) {
     gemv_gguf(type, W, rows, K, xq, ncols, nullptr, y, rows, bound, nullptr);
+    return 0;
+  }
+  if (type == kTypeQ5KPlanar) {
+    std::vector<uint8_t> g((size_t)(rows * (K / kQK) * kQ5KBytes));
+    unpack_planar_q5(W, rows, K, g.data());
+    gemv_gguf(kTypeQ5K, g.data(), rows, K, xq, ncols, nullptr, y, rows, bound, nullptr);
     return 0;
   }
   if (type == kTypeQ6KPlanar) {
@@ -517,8 +618,14 @@ int orc_block_sums(int type, const uint8_t* W, int64_t rows, int K, const uint8_
                    int32_t* sumi) {
   if (rows <= 0 || K <= 0 || K % kQK != 0 || ncols < 1) return -2;
   std::vector<float> y((size_t)(ncols * rows));
-  if (type == kTypeQ6K || type == kTypeQ4K) {
+  if (type == kTypeQ6K || type == kTypeQ4K || type == kTypeQ5K) {
     gemv_gguf(type, W, rows, K, xq, ncols, nullptr, y.data(), rows, nullptr, sumi);
+    return 0;
+  }
+  if (type == kTypeQ5KPlanar) {
+    std::vector<uint8_t> g((size_t)(rows * (K / kQK) * kQ5KBytes));
+    unpack_planar_q5(W, rows, K, g.data());
+    gemv_gguf(kTypeQ5K, g.data(), rows, K, xq, ncols, nullptr, y.data(), rows, nullptr, sumi);
     return 0;
   }
   if (type == kTypeQ6KPlanar) {
@@ -585,8 +692,6 @@ int orc_grouped(int type, const uint8_t* W, int n_experts, int64_t rows, int K,
   return 0;
 }
 
-// gu: [n][2F] rows laid out [gate F | up F].  h = g/(1+exp(-g)) * u in fp32,
-// then Q8_1 per 32 into xq [n][F/32].  h_out (may be NULL): [n][F].
 // RMSNorm then Q8_1, per column: the step before the activation quantiser
 // when the norm is folded into it ("Strata" PR #1774 "How it was checked": the opt-in
 // STRATA_GR_FUSE_NORM, #1775; the pages give no formula, so this is the
@@ -614,6 +719,8 @@ int orc_rmsnorm_quantize_q8_1(const float* x, const float* w, float eps, int K, 
   return 0;
 }
 
+// gu: [n][2F] rows laid out [gate F | up F].  h = g/(1+exp(-g)) * u in fp32,
+// then Q8_1 per 32 into xq [n][F/32].  h_out (may be NULL): [n][F].
 int orc_silu_mul_quantize(const float* gu, int F, int n, uint8_t* xq, float* h_out) {
   if (F <= 0 || F % kQK8 != 0 || n < 0) return -2;
   std::vector<float> h((size_t)F);

@@ -9,6 +9,10 @@ nibble for r < 2, high nibble for r >= 2) and its high 2 bits to
 qh[32h + l] at bit 2r.  Scale index n // 16, block layout
 ql[128] | qh[64] | int8 scales[16] | fp16 d.
 
+Q5_K (GGUF arrangement): d | dmin | the Q4_K scale bytes | qh[32] | qs[128];
+weight n = 32j + l (sub-block j) keeps its low 4 bits where Q4_K would and
+its fifth bit in bit j of qh[l].
+
 Q4_K (GGUF arrangement): d | dmin | 12 packed scale bytes | qs[128]; the
 scales of sub-blocks 0-3 and mins of 0-3 take the low 6 bits of bytes 0-3 and
 4-7; sub-blocks 4-7 keep their low 4 bits of scale and min in bytes 8-11
@@ -61,6 +65,34 @@ def encode_q4_k(q: np.ndarray, sc: np.ndarray, m: np.ndarray, d, dmin) -> np.nda
     out[2:4] = f16_bytes(dmin)
     out[4:16] = s
     out[16:144] = qs
+    return out
+
+
+def _pack_scales_mins(sc, m) -> np.ndarray:
+    sc = np.asarray(sc, dtype=np.int64)
+    m = np.asarray(m, dtype=np.int64)
+    s = np.zeros(12, dtype=np.int64)
+    s[0:4] = sc[0:4] | ((sc[4:8] >> 4) << 6)
+    s[4:8] = m[0:4] | ((m[4:8] >> 4) << 6)
+    s[8:12] = (sc[4:8] & 15) | ((m[4:8] & 15) << 4)
+    return s
+
+
+def encode_q5_k(q: np.ndarray, sc: np.ndarray, m: np.ndarray, d, dmin) -> np.ndarray:
+    """q: 256 codes in 0..31; sc, m: 8 values in 0..63."""
+    q = np.asarray(q, dtype=np.int64)
+    n = np.arange(256)
+    j, l = n // 32, n % 32
+    qs = np.zeros(128, dtype=np.int64)
+    np.add.at(qs, 32 * (j // 2) + l, (q & 15) << (4 * (j % 2)))
+    qh = np.zeros(32, dtype=np.int64)
+    np.add.at(qh, l, (q >> 4) << j)
+    out = np.zeros(176, dtype=np.uint8)
+    out[0:2] = f16_bytes(d)
+    out[2:4] = f16_bytes(dmin)
+    out[4:16] = _pack_scales_mins(sc, m)
+    out[16:48] = qh
+    out[48:176] = qs
     return out
 
 
