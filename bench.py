@@ -62,6 +62,8 @@ def workload_cases(name):
                 ("q6_k_planar_draft", DRAFT_ROWS, HEAD_SHAPE[1], [1, 2, 3, 4, 5])]
     if name == "q4k_dense":
         return [("q4_k_planar", r, k, [1, 4]) for r, k in Q4K_SHAPES]
+    if name == "q5k_dense":
+        return [("q5_k_planar", r, k, [1, 4]) for r, k in Q4K_SHAPES]
     if name == "q4k_dense_gguf":
         return [("q4_k", r, k, [1, 4]) for r, k in Q4K_SHAPES]
     raise SystemExit(f"unknown workload {name}")
@@ -73,6 +75,7 @@ WORKLOAD_DESC = {
     "lm_head": "Q6_K LM head 151936x2560 at 1-5 cols, planar tiles; 4096-row draft head gathered from it",
     "q4k_dense": "Q4_K dense 12288x2560, 6144x2560, 2560x6144, 640x2560, 512x2560 at 1 and 4 cols, planar tiles",
     "q4k_dense_gguf": "Q4_K dense 12288x2560, 6144x2560, 2560x6144, 640x2560, 512x2560 at 1 and 4 cols, GGUF blocks",
+    "q5k_dense": "Q5_K dense 12288x2560, 6144x2560, 2560x6144, 640x2560, 512x2560 at 1 and 4 cols, planar tiles",
     "moe_t1": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=1 top-8 (planar experts)",
     "moe_t4": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=4 top-8 (planar experts)",
     "moe_t8": "grouped MoE Q4_K, 256 experts, gate|up 1536x2560, down 2560x768, T=8 top-8 (planar experts)",
@@ -116,6 +119,20 @@ def profiled_traffic(summary: str):
     """DRAM bytes per MMVQ launch from a committed ncu summary (or None)."""
     v = profiled_field(summary, "traffic_bytes_per_mmvq_launch")
     return None if v is None else int(v)
+
+
+def host_weights_for(fmt: str, rows: int, K: int, salt: int = 0):
+    """Seeded GGUF blocks for a workload format (the planar forms repack them)."""
+    from block_quantized_matvec_gb300 import synth
+    gen = (synth.q4_k_weights if fmt.startswith("q4_k") else
+           synth.q5_k_weights if fmt.startswith("q5_k") else synth.q6_k_weights)
+    return gen(rows, K, salt=salt)
+
+
+def repack_source(fmt: str) -> int:
+    from block_quantized_matvec_gb300 import mmvq
+    return (mmvq.TYPE_Q4_K if fmt.startswith("q4_k") else
+            mmvq.TYPE_Q5_K if fmt.startswith("q5_k") else mmvq.TYPE_Q6_K)
 
 
 def max_over_ranks(value: float, world: int, device) -> float:
@@ -246,7 +263,8 @@ def run_ours(args, rank, world, local_rank):
 
     cases_spec = workload_cases(args.workload)
     type_of = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K,
-               "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR, "q6_k_planar_draft": mmvq.TYPE_Q6_K_PLANAR}
+               "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR, "q6_k_planar_draft": mmvq.TYPE_Q6_K_PLANAR,
+               "q5_k_planar": mmvq.TYPE_Q5_K_PLANAR}
 
     # resident weights: copies per shape so that each shape's copies exceed 2x L2
     mats = []
@@ -260,13 +278,11 @@ def run_ours(args, rank, world, local_rank):
                                             torch.from_numpy(ids).to(dev))
             host_weights.append(np.ascontiguousarray(host_weights[0][ids]))
         else:
-            gen = synth.q4_k_weights if fmt.startswith("q4_k") else synth.q6_k_weights
-            W = gen(rows, K, salt=si)
+            W = host_weights_for(fmt, rows, K, salt=si)
             host_weights.append(W)
             Wd = torch.from_numpy(W.reshape(-1)).to(dev)
-            if fmt in ("q6_k_planar", "q4_k_planar"):
-                Wd = mmvq.repack_planar(Wd, rows, K, type_=mmvq.TYPE_Q4_K if fmt == "q4_k_planar"
-                                        else mmvq.TYPE_Q6_K)
+            if fmt.endswith("_planar"):
+                Wd = mmvq.repack_planar(Wd, rows, K, type_=repack_source(fmt))
         nbytes = metrics.weight_bytes(fmt, rows, K)
         copies = max(2, math.ceil(2 * l2 / nbytes))
         mats.append([Wd] + [Wd.clone() for _ in range(copies - 1)])
@@ -693,7 +709,8 @@ def _oracle_pass(cases_spec, host_weights, row_sample, salt0=0):
     import oracle
     from block_quantized_matvec_gb300 import metrics, synth
     tcode = {"q6_k_planar": oracle.TYPE_Q6_K, "q6_k": oracle.TYPE_Q6_K, "q4_k": oracle.TYPE_Q4_K,
-             "q4_k_planar": oracle.TYPE_Q4_K, "q6_k_planar_draft": oracle.TYPE_Q6_K}
+             "q4_k_planar": oracle.TYPE_Q4_K, "q6_k_planar_draft": oracle.TYPE_Q6_K,
+             "q5_k_planar": oracle.TYPE_Q5_K}
     nbytes = 0
     secs = 0.0
     for si, (fmt, rows, K, cols) in enumerate(cases_spec):
@@ -736,8 +753,8 @@ def run_reference(args, rank, world):
     sample_rows = 64
     host_weights = []
     for si, (fmt, rows, K, cols) in enumerate(cases_spec):
-        gen = synth.q4_k_weights if fmt.startswith("q4_k") else synth.q6_k_weights
-        host_weights.append(np.ascontiguousarray(gen(min(rows, sample_rows), K, salt=si)))
+        host_weights.append(np.ascontiguousarray(host_weights_for(fmt, min(rows, sample_rows), K,
+                                                                  salt=si)))
     for _ in range(args.warmup):
         _oracle_pass(cases_spec, host_weights, sample_rows)
     nb_total, s_total = 0, 0.0
@@ -768,11 +785,11 @@ def run_case_for_profile(spec: str, launches: int):
     fmt, shape, nc = spec.split(":")
     rows, K = (int(v) for v in shape.split("x"))
     nc = int(nc)
-    t = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K}[fmt]
-    gen = synth.q4_k_weights if fmt == "q4_k" else synth.q6_k_weights
-    W = torch.from_numpy(gen(rows, K).reshape(-1)).cuda()
-    if fmt == "q6_k_planar":
-        W = mmvq.repack_planar(W, rows, K)
+    t = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K,
+         "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR, "q5_k_planar": mmvq.TYPE_Q5_K_PLANAR}[fmt]
+    W = torch.from_numpy(host_weights_for(fmt, rows, K).reshape(-1)).cuda()
+    if fmt.endswith("_planar"):
+        W = mmvq.repack_planar(W, rows, K, type_=repack_source(fmt))
     xq = mmvq.quantize_q8_1(torch.from_numpy(synth.activations(K, nc)).cuda())
     y = torch.empty((nc, rows), device="cuda")
     for _ in range(launches):

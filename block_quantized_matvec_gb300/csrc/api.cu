@@ -89,7 +89,21 @@ int mmvq_quantize_route_groups(const float* x, int K, int ncols, int64_t ldx, vo
 
 static bool dense_type(int type) {
   return type == MMVQ_Q4_K || type == MMVQ_Q6_K || type == MMVQ_Q4_K_PLANAR ||
+         type == MMVQ_Q6_K_PLANAR || type == MMVQ_Q5_K_PLANAR;
+}
+
+static bool grouped_type(int type) {
+  return type == MMVQ_Q4_K || type == MMVQ_Q6_K || type == MMVQ_Q4_K_PLANAR ||
          type == MMVQ_Q6_K_PLANAR;
+}
+
+static bool repack_source_type(int type) {
+  return type == MMVQ_Q6_K || type == MMVQ_Q4_K || type == MMVQ_Q5_K;
+}
+
+static int tile_bytes_of_source(int type) {
+  return type == MMVQ_Q4_K ? mmvq::kTileBytesQ4
+                           : type == MMVQ_Q5_K ? mmvq::kTileBytesQ5 : mmvq::kTileBytes;
 }
 
 static int gemv_checks(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
@@ -131,7 +145,7 @@ int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, i
                  const int32_t* expert_ids, const int32_t* token_offsets, int n_groups,
                  const int32_t* act_index, const void* xq, int n_xq_cols, float* y,
                  int32_t* status, mmvq_stream_t stream) {
-  if (!dense_type(type)) return MMVQ_ERR_TYPE;
+  if (!grouped_type(type)) return MMVQ_ERR_TYPE;
   if (!W_experts || !expert_ids || !token_offsets || !xq || !y) return MMVQ_ERR_NULL;
   int rc = check_weights_shape(rows, K);
   if (rc) return rc;
@@ -170,19 +184,19 @@ int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq, float* 
 }
 
 int64_t mmvq_planar_bytes(int type, int64_t rows, int K) {
-  if (type != MMVQ_Q6_K && type != MMVQ_Q4_K) return -1;
+  if (!repack_source_type(type)) return -1;
   if (check_weights_shape(rows, K) != MMVQ_OK) return -1;
   const int64_t groups = (rows + mmvq::kTileRows - 1) / mmvq::kTileRows;
-  return groups * (K / mmvq::kQK) * (type == MMVQ_Q4_K ? mmvq::kTileBytesQ4 : mmvq::kTileBytes);
+  return groups * (K / mmvq::kQK) * tile_bytes_of_source(type);
 }
 
 int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int K, void* W_planar,
                        mmvq_stream_t stream) {
-  if (type != MMVQ_Q6_K && type != MMVQ_Q4_K) return MMVQ_ERR_TYPE;
+  if (!repack_source_type(type)) return MMVQ_ERR_TYPE;
   if (!W_gguf || !W_planar) return MMVQ_ERR_NULL;
   const int rc = check_weights_shape(rows, K);
   if (rc) return rc;
-  if (!aligned(W_gguf, type == MMVQ_Q4_K ? 16 : 2) || !aligned(W_planar, 16)) return MMVQ_ERR_ALIGN;
+  if (!aligned(W_gguf, type == MMVQ_Q6_K ? 2 : 16) || !aligned(W_planar, 16)) return MMVQ_ERR_ALIGN;
   return mmvq::launch_repack_planar(type, W_gguf, rows, K, W_planar, (cudaStream_t)stream);
 }
 

@@ -14,13 +14,15 @@ constexpr int kQK8 = 32;          // values per Q8_1 block
 constexpr int kQ81Bytes = 36;     // fp16 d, fp16 s, int8 q[32]
 constexpr int kQ6KBytes = 210;
 constexpr int kQ4KBytes = 144;
+constexpr int kQ5KBytes = 176;
 constexpr int kTileRows = 16;     // rows per planar tile / per warp
 constexpr int kTileBytes = 3360;  // 16 rows x one Q6_K block
 constexpr int kTileBytesQ4 = 2304;  // 16 rows x one Q4_K block
+constexpr int kTileBytesQ5 = 2816;  // 16 rows x one Q5_K block
 constexpr int kMaxCols = 8;
 
 // Weight layouts the kernels read.
-enum Layout { kQ6Planar = 0, kQ6Gguf = 1, kQ4Gguf = 2, kQ4Planar = 3 };
+enum Layout { kQ6Planar = 0, kQ6Gguf = 1, kQ4Gguf = 2, kQ4Planar = 3, kQ5Planar = 4 };
 constexpr int kMaxK = 16384;
 
 // Activation quants in shared memory: per column, K bytes with 16 bytes of

@@ -169,10 +169,13 @@ __device__ __forceinline__ void q4_scale_min(const uint32_t (&hdr)[4], int j, in
 
 // One lane's 128 weights (sub-blocks 4u..4u+3) of block b against NCOLS
 // columns: acc[c] += d * sum d_a*sumi - dmin * sum s_a*m.
-template <int NCOLS>
-__device__ __forceinline__ void q4_dot(const Q4Half& w, int u, int b, const uint8_t* act, int rb,
-                                       const float* da, const float* sa, int nbq,
-                                       float (&acc)[NCOLS], int32_t* sumi_out, int64_t sumi_cs) {
+// FIFTH (Q5_K): the code's fifth bit, bit 4u+s of qh byte l, is added to
+// the nibble of sub-block 4u+s (qh: the block's 32 qh bytes as 8 words).
+template <int NCOLS, bool FIFTH>
+__device__ __forceinline__ void q45_dot(const Q4Half& w, const uint32_t* qh, int u, int b,
+                                        const uint8_t* act, int rb, const float* da,
+                                        const float* sa, int nbq, float (&acc)[NCOLS],
+                                        int32_t* sumi_out, int64_t sumi_cs) {
   float inner_d[NCOLS], inner_m[NCOLS];
 #pragma unroll
   for (int c = 0; c < NCOLS; ++c) {
@@ -194,6 +197,7 @@ __device__ __forceinline__ void q4_dot(const Q4Half& w, int u, int b, const uint
       uint32_t v = w.qs[8 * (s >> 1) + k];
       if (s & 1) v >>= 4;
       wv[k] = (int)(v & 0x0f0f0f0fu);
+      if (FIFTH) wv[k] |= (int)(((qh[k] >> (4 * u + s)) & 0x01010101u) << 4);
     }
     const int kb = 8 * b + 4 * u + s;
     const float mf = (float)m;
@@ -220,6 +224,44 @@ __device__ __forceinline__ void q4_dot(const Q4Half& w, int u, int b, const uint
   const float dmin = half_bits_to_float((uint16_t)(w.hdr[0] >> 16));
 #pragma unroll
   for (int c = 0; c < NCOLS; ++c) acc[c] = fmaf(d, inner_d[c], fmaf(-dmin, inner_m[c], acc[c]));
+}
+
+template <int NCOLS>
+__device__ __forceinline__ void q4_dot(const Q4Half& w, int u, int b, const uint8_t* act, int rb,
+                                       const float* da, const float* sa, int nbq,
+                                       float (&acc)[NCOLS], int32_t* sumi_out, int64_t sumi_cs) {
+  q45_dot<NCOLS, false>(w, nullptr, u, b, act, rb, da, sa, nbq, acc, sumi_out, sumi_cs);
+}
+
+// ----------------------------------------------------------------- Q5_K ----
+// A Q5_K block half is a Q4_K half plus the block's qh bytes (every lane of
+// a row needs all 32: bit 4u+s of qh[l] belongs to sub-block 4u+s).
+struct Q5Half {
+  Q4Half q4;
+  uint32_t qh[8];
+};
+
+// Planar Q5_K tile in shared memory: qs and header as the Q4_K tile, the
+// row's qh at [2304 + 32i, +32).
+__device__ __forceinline__ void load_q5_tile_smem(const uint8_t* tile, int lane, Q5Half& w) {
+  load_q4_tile_smem(tile, lane, w.q4);
+  const uint4* hp = reinterpret_cast<const uint4*>(tile + 2304 + 32 * (lane & 15));
+  const uint4 h0 = hp[0], h1 = hp[1];
+  w.qh[0] = h0.x;
+  w.qh[1] = h0.y;
+  w.qh[2] = h0.z;
+  w.qh[3] = h0.w;
+  w.qh[4] = h1.x;
+  w.qh[5] = h1.y;
+  w.qh[6] = h1.z;
+  w.qh[7] = h1.w;
+}
+
+template <int NCOLS>
+__device__ __forceinline__ void q5_dot(const Q5Half& w, int u, int b, const uint8_t* act, int rb,
+                                       const float* da, const float* sa, int nbq,
+                                       float (&acc)[NCOLS], int32_t* sumi_out, int64_t sumi_cs) {
+  q45_dot<NCOLS, true>(w.q4, w.qh, u, b, act, rb, da, sa, nbq, acc, sumi_out, sumi_cs);
 }
 
 }  // namespace mmvq

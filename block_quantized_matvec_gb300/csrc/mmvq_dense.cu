@@ -288,7 +288,8 @@ int planar_tma_shape(int type, int64_t rows, int K, int ncols, int32_t* info);
 int dense_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
   switch (type) {
     case MMVQ_Q6_K_PLANAR:
-    case MMVQ_Q4_K_PLANAR: return planar_tma_shape(type, rows, K, ncols, info);
+    case MMVQ_Q4_K_PLANAR:
+    case MMVQ_Q5_K_PLANAR: return planar_tma_shape(type, rows, K, ncols, info);
     case MMVQ_Q6_K: return dense_shape_layout<kQ6Gguf>(rows, K, ncols, info);
     case MMVQ_Q4_K: return dense_shape_layout<kQ4Gguf>(rows, K, ncols, info);
   }
@@ -304,7 +305,8 @@ int launch_dense(int type, const void* W, int64_t rows, int K, const void* xq, i
   const uint8_t* x = static_cast<const uint8_t*>(xq);
   switch (type) {
     case MMVQ_Q6_K_PLANAR:
-    case MMVQ_Q4_K_PLANAR: return launch_planar_tma(type, W, rows, K, xq, ncols, y, sumi, flags, s);
+    case MMVQ_Q4_K_PLANAR:
+    case MMVQ_Q5_K_PLANAR: return launch_planar_tma(type, W, rows, K, xq, ncols, y, sumi, flags, s);
     case MMVQ_Q6_K: return launch_dense_layout<kQ6Gguf>(w, rows, K, x, ncols, y, sumi, s);
     case MMVQ_Q4_K: return launch_dense_layout<kQ4Gguf>(w, rows, K, x, ncols, y, sumi, s);
   }

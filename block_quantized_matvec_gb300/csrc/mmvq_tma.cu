@@ -130,13 +130,18 @@ __device__ __forceinline__ void load_q6_tile_smem(const uint8_t* tile, int lane,
 // (S stages of G*P tiles, 128-byte aligned), the activation quants, d_a as
 // floats, the K-slice partials [C][8][16].
 __host__ __device__ inline size_t tma_ring_offset(int S) { return ((size_t)16 * S + 16 + 127) & ~size_t(127); }
+// Layouts whose blocks carry a min term (d*sc*q - dmin*m): the Q8_1 sums s
+// are staged beside d.
+__host__ __device__ constexpr bool has_min(int layout) {
+  return layout == kQ4Planar || layout == kQ5Planar;
+}
 __host__ __device__ constexpr int tile_bytes(int layout) {
-  return layout == kQ4Planar ? kTileBytesQ4 : kTileBytes;
+  return layout == kQ4Planar ? kTileBytesQ4 : layout == kQ5Planar ? kTileBytesQ5 : kTileBytes;
 }
 __host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int ncols, int G, int P) {
   const int C = G * P;
   return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + (size_t)ncols * act_row_bytes(K) +
-         (size_t)ncols * (K / kQK8) * 4 * (layout == kQ4Planar ? 2 : 1) +
+         (size_t)ncols * (K / kQK8) * 4 * (has_min(layout) ? 2 : 1) +
          (size_t)C * kMaxCols * kTileRows * 4;
 }
 
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   uint8_t* act = ring + (size_t)S * stage_bytes;
   float* da = reinterpret_cast<float*>(act + NCOLS * rb);
   float* sa = da + NCOLS * nbq;  // Q4_K only
-  float* red = sa + (LAYOUT == kQ4Planar ? NCOLS * nbq : 0);
+  float* red = sa + (has_min(LAYOUT) ? NCOLS * nbq : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -245,7 +250,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   bool waited = !stable;
   if (!stable) grid_dependency_wait();
   stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da,
-             LAYOUT == kQ4Planar ? sa : nullptr, tid, nthreads);
+             has_min(LAYOUT) ? sa : nullptr, tid, nthreads);
   group_sync(1, nthreads);
 
   const int g = warp / P;
@@ -284,6 +289,12 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (valid) q4_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, rows * nbq);
+      } else if (LAYOUT == kQ5Planar) {
+        Q5Half w;
+        if (valid) load_q5_tile_smem(tile, lane, w);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (valid) q5_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, rows * nbq);
       } else {
         Q6Half w;
         if (valid) load_q6_tile_smem(tile, lane, w);
@@ -769,6 +780,8 @@ int launch_planar_tma(int type, const void* W, int64_t rows, int K, const void* 
   const uint8_t* x = static_cast<const uint8_t*>(xq);
   if (type == MMVQ_Q4_K_PLANAR)
     return launch_tma_layout<kQ4Planar>(w, rows, K, x, ncols, y, sumi, flags, s);
+  if (type == MMVQ_Q5_K_PLANAR)
+    return launch_tma_layout<kQ5Planar>(w, rows, K, x, ncols, y, sumi, flags, s);
   return launch_tma_layout<kQ6Planar>(w, rows, K, x, ncols, y, sumi, flags, s);
 }
 
@@ -803,6 +816,7 @@ static int tma_shape_layout(int64_t rows, int K, int ncols, int32_t* info) {
 
 int planar_tma_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
   if (type == MMVQ_Q4_K_PLANAR) return tma_shape_layout<kQ4Planar>(rows, K, ncols, info);
+  if (type == MMVQ_Q5_K_PLANAR) return tma_shape_layout<kQ5Planar>(rows, K, ncols, info);
   return tma_shape_layout<kQ6Planar>(rows, K, ncols, info);
 }
 

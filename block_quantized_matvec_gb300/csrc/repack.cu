@@ -103,6 +103,36 @@ __global__ void __launch_bounds__(256) repack_planar_q4_kernel(const uint8_t* __
   *reinterpret_cast<uint4*>(P + t * kTileBytesQ4 + 16 * q) = v;
 }
 
+// Q5_K blocks -> planar Q5_K tiles (include/mmvq.h): one thread per 16-byte
+// vector of the 2816-byte tile: 128 qs vectors, 16 headers, 32 qh halves.
+__global__ void __launch_bounds__(256) repack_planar_q5_kernel(const uint8_t* __restrict__ W,
+                                                               int64_t rows, int nb,
+                                                               uint8_t* __restrict__ P) {
+  // Writes weights: no early launch of the next kernel.
+  grid_dependency_wait();
+  const int64_t t = blockIdx.x;
+  const int64_t g = t / nb;
+  const int b = (int)(t - g * nb);
+  const int q = threadIdx.x;
+  if (q >= kTileBytesQ5 / 16) return;
+  int i, off;
+  if (q < 128) {  // qs[64u + 16j ..] of lane L = 16u + i at 512j + 16L
+    const int j = q >> 5, L = q & 31;
+    i = L & 15;
+    off = 48 + 64 * (L >> 4) + 16 * j;
+  } else if (q < 144) {  // header of row i at 2048 + 16i
+    i = q - 128;
+    off = 0;
+  } else {  // qh half of row i at 2304 + 32i + 16 * half
+    i = (q - 144) >> 1;
+    off = 16 + 16 * ((q - 144) & 1);
+  }
+  const int64_t row = g * kTileRows + i;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (row < rows) v = *reinterpret_cast<const uint4*>(W + (row * nb + b) * kQ5KBytes + off);
+  *reinterpret_cast<uint4*>(P + t * kTileBytesQ5 + 16 * q) = v;
+}
+
 // One CTA per output tile; out row k = source row row_ids[k] (zero bytes
 // for k >= n or an invalid id).
 __global__ void __launch_bounds__(256) gather_planar_kernel(const uint8_t* __restrict__ P,
@@ -183,6 +213,9 @@ int launch_repack_planar(int type, const void* W, int64_t rows, int K, void* P, 
   if (tiles > 0x7fffffff) return MMVQ_ERR_SHAPE;
   if (type == MMVQ_Q4_K)
     return launch_pdl(repack_planar_q4_kernel, dim3((unsigned)tiles), dim3(256), 0, s,
+                      static_cast<const uint8_t*>(W), rows, nb, static_cast<uint8_t*>(P));
+  if (type == MMVQ_Q5_K)
+    return launch_pdl(repack_planar_q5_kernel, dim3((unsigned)tiles), dim3(256), 0, s,
                       static_cast<const uint8_t*>(W), rows, nb, static_cast<uint8_t*>(P));
   return launch_pdl(repack_planar_kernel, dim3((unsigned)tiles), dim3(256), 0, s,
                     static_cast<const uint8_t*>(W), rows, nb, static_cast<uint8_t*>(P));

@@ -9,7 +9,7 @@ bytes of the distinct experts actually read.
 from __future__ import annotations
 
 BYTES_PER_256 = {"q6_k": 210, "q6_k_planar": 210, "q6_k_planar_draft": 210, "q4_k": 144,
-                 "q4_k_planar": 144, "iq3_s": 110}
+                 "q4_k_planar": 144, "q5_k": 176, "q5_k_planar": 176, "iq3_s": 110}
 Q8_1_BYTES_PER_32 = 36
 
 

@@ -20,7 +20,10 @@ TYPE_Q4_K = 12
 TYPE_Q6_K = 14
 TYPE_Q6_K_PLANAR = 1014
 TYPE_Q4_K_PLANAR = 1012
-BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210, TYPE_Q6_K_PLANAR: 210, TYPE_Q4_K_PLANAR: 144}
+TYPE_Q5_K = 13
+TYPE_Q5_K_PLANAR = 1013
+BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210, TYPE_Q6_K_PLANAR: 210, TYPE_Q4_K_PLANAR: 144,
+               TYPE_Q5_K: 176, TYPE_Q5_K_PLANAR: 176}
 Q8_1_BYTES = 36
 MAX_COLS = 8
 
@@ -226,7 +229,7 @@ def launch_shape(type_: int, rows: int, K: int, ncols: int) -> dict:
     info = (ctypes.c_int32 * 6)()
     _check(lib().mmvq_launch_shape(type_, rows, K, ncols, info), "mmvq_launch_shape")
     keys = (["grid", "threads", "smem", "G", "P", "stages"]
-            if type_ in (TYPE_Q6_K_PLANAR, TYPE_Q4_K_PLANAR)
+            if type_ in (TYPE_Q6_K_PLANAR, TYPE_Q4_K_PLANAR, TYPE_Q5_K_PLANAR)
             else ["grid", "threads", "smem", "WR", "WK", "unused"])
     return dict(zip(keys, list(info)))
 

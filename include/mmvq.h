@@ -55,6 +55,15 @@
  *      bytes [512*j + 16*L, +16)  j = 0..3 : qs[64*u + 16*j .. +15]
  *      bytes [2048 + 16*i, +16)            : d, dmin, scales[12] of row i
  *    Size: mmvq_planar_bytes(MMVQ_Q4_K, rows, K).
+ *  - Q5_K block, 176 bytes per 256 weights (the pages run Q5_K matrices in
+ *    the same wide kernels, PR #2340 "ld_i4_a4", without giving the block;
+ *    this is the GGUF Q5_K arrangement): fp16 d, fp16 dmin, the Q4_K scale
+ *    and min bytes, qh[32], qs[128] as in Q4_K; weight l of sub-block j
+ *    takes its fifth bit from bit j of qh[l]; code q in 0..31,
+ *    weight = d * sc * q - dmin * m.  Products run from planar tiles only.
+ *  - Planar Q5_K (MMVQ_Q5_K_PLANAR): 2816-byte tiles, the Q4_K tile plus
+ *      bytes [2304 + 32*i, +32)            : qh[0..31] of row i
+ *    Size: mmvq_planar_bytes(MMVQ_Q5_K, rows, K).
  *
  * Results: y is fp32, [ncols][rows] (column-major over the activation
  * columns).  Block sums are exact integers; the FP32 output of a row is
@@ -83,8 +92,10 @@ typedef struct CUstream_st* mmvq_stream_t; /* == cudaStream_t */
 
 enum mmvq_type {
   MMVQ_Q4_K = 12,          /* GGUF Q4_K blocks, 144 B / 256 weights */
+  MMVQ_Q5_K = 13,          /* GGUF Q5_K blocks, 176 B / 256 weights (repack source) */
   MMVQ_Q6_K = 14,          /* GGUF Q6_K blocks, 210 B / 256 weights */
   MMVQ_Q4_K_PLANAR = 1012, /* Q4_K in 16-row planar tiles (see above) */
+  MMVQ_Q5_K_PLANAR = 1013, /* Q5_K in 16-row planar tiles (see above) */
   MMVQ_Q6_K_PLANAR = 1014  /* Q6_K in 16-row planar tiles (see above) */
 };
 
@@ -130,7 +141,8 @@ MMVQ_API int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, v
 /*
  * Dense MMVQ (PR #2207 wide kernels, PR #1774 iq3s_wide_kernel: weights read
  * once for all 1-8 columns).  W: rows x K/256 blocks of `type` (MMVQ_Q4_K,
- * MMVQ_Q6_K, MMVQ_Q4_K_PLANAR or MMVQ_Q6_K_PLANAR); xq: [ncols][K/32] Q8_1 blocks;
+ * MMVQ_Q6_K, MMVQ_Q4_K_PLANAR, MMVQ_Q5_K_PLANAR or MMVQ_Q6_K_PLANAR); xq:
+ * [ncols][K/32] Q8_1 blocks;
  * y: fp32 [ncols][rows].  Requires K % 256 == 0 (PR #1774: the row length a
  * multiple of 256), 1 <= ncols <= 8 (PR #2207: 1 to 8 columns),
  * K <= 16384, 1 <= rows <= 2^31 - 1.
@@ -234,16 +246,17 @@ MMVQ_API int mmvq_rmsnorm_quantize_q8_1(const float* x, const float* w, float ep
                                         int64_t ldx, void* xq, float* y_out,
                                         mmvq_stream_t stream);
 
-/* Bytes of the planar form of a rows x K matrix of `type` (MMVQ_Q6_K or
- * MMVQ_Q4_K); -1 on a bad type or shape. */
+/* Bytes of the planar form of a rows x K matrix of `type` (MMVQ_Q6_K,
+ * MMVQ_Q5_K or MMVQ_Q4_K); -1 on a bad type or shape. */
 MMVQ_API int64_t mmvq_planar_bytes(int type, int64_t rows, int K);
 
 /*
  * Load-time repack of GGUF Q6_K blocks into planar tiles (PR #2340
  * "STRATA_Q6_PLANAR": same bytes, the GGUF copy can then be freed).
  * Out-of-place; W_planar holds mmvq_planar_bytes(type, rows, K) bytes; pad
- * rows are written as zeros.  type: MMVQ_Q6_K (-> MMVQ_Q6_K_PLANAR) or
- * MMVQ_Q4_K (-> MMVQ_Q4_K_PLANAR).  K % 256 == 0.
+ * rows are written as zeros.  type: MMVQ_Q6_K (-> MMVQ_Q6_K_PLANAR),
+ * MMVQ_Q5_K (-> MMVQ_Q5_K_PLANAR) or MMVQ_Q4_K (-> MMVQ_Q4_K_PLANAR).
+ * K % 256 == 0; W_gguf 16-byte aligned (2-byte for Q6_K).
  */
 MMVQ_API int mmvq_repack_planar(int type, const void* W_gguf, int64_t rows, int K, void* W_planar,
                        mmvq_stream_t stream);

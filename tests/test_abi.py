@@ -46,6 +46,7 @@ def test_planar_bytes_host_only(lib):
     assert mmvq.planar_bytes(151936, 2560) == 151936 // 16 * 10 * 3360 == 151936 * 10 * 210
     assert mmvq.planar_bytes(17, 256) == 2 * 1 * 3360
     assert mmvq.planar_bytes(17, 512, mmvq.TYPE_Q4_K) == 2 * 2 * 2304
+    assert mmvq.planar_bytes(17, 512, mmvq.TYPE_Q5_K) == 2 * 2 * 2816 == 32 * 2 * 176
     assert lib.mmvq_planar_bytes(14, 16, 100) == -1
     assert lib.mmvq_planar_bytes(14, 0, 256) == -1
     assert lib.mmvq_planar_bytes(1014, 16, 256) == -1
@@ -70,6 +71,9 @@ A = 0x10000  # an aligned fake device address: never dereferenced, calls fail be
     ((12, A, 16, 256, A, 1, A + 2, None), mmvq.ERR_ALIGN),
     ((1012, A + 4, 16, 256, A, 1, A, None), mmvq.ERR_ALIGN),
     ((1012, A, 16, 200, A, 1, A, None), mmvq.ERR_SHAPE),
+    ((13, A, 16, 256, A, 1, A, None), mmvq.ERR_TYPE),          # Q5_K runs from planar tiles
+    ((1013, A + 8, 16, 256, A, 1, A, None), mmvq.ERR_ALIGN),
+    ((1013, A, 16, 256, A, 9, A, None), mmvq.ERR_NCOLS),
 ])
 def test_gemv_rejects_bad_arguments_on_host(lib, args, code):
     assert lib.mmvq_gemv(*args) == code
@@ -86,6 +90,7 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_grouped(1012, A, 256, 1530, 2560, A, A, 256, A, A, 1, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_grouped(1014, A, 256, 1530, 2560, A, A, 256, A, A, 1, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_grouped(*g[:0], 99, *g[1:]) == mmvq.ERR_TYPE
+    assert L.mmvq_grouped(*g[:0], 1013, *g[1:]) == mmvq.ERR_TYPE
     assert L.mmvq_grouped(*g[:7], 0, *g[8:]) == mmvq.ERR_ROUTING
     assert L.mmvq_grouped(*g[:7], 4097, *g[8:]) == mmvq.ERR_ROUTING
     assert L.mmvq_grouped(*g[:4], 2560 + 32, *g[5:]) == mmvq.ERR_SHAPE
@@ -113,6 +118,8 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_silu_mul_quantize_q8_1(A, 768, 0, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_repack_planar(99, A, 16, 256, A, None) == mmvq.ERR_TYPE
     assert L.mmvq_repack_planar(12, A + 8, 16, 256, A, None) == mmvq.ERR_ALIGN
+    assert L.mmvq_repack_planar(13, A + 8, 16, 256, A, None) == mmvq.ERR_ALIGN
+    assert L.mmvq_repack_planar(1013, A, 16, 256, A, None) == mmvq.ERR_TYPE
     assert L.mmvq_repack_planar(14, A, 16, 256, A + 8, None) == mmvq.ERR_ALIGN
     assert L.mmvq_gather_planar_rows(A, 16, 256, A, 0, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_gather_planar_rows(A, 16, 256, A, 4, A + 8, None, None) == mmvq.ERR_ALIGN

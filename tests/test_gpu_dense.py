@@ -20,6 +20,7 @@ KINDS = {
     "q6_k_planar": (mmvq.TYPE_Q6_K_PLANAR, oracle.TYPE_Q6_K, synth.q6_k_weights),
     "q4_k": (mmvq.TYPE_Q4_K, oracle.TYPE_Q4_K, synth.q4_k_weights),
     "q4_k_planar": (mmvq.TYPE_Q4_K_PLANAR, oracle.TYPE_Q4_K, synth.q4_k_weights),
+    "q5_k_planar": (mmvq.TYPE_Q5_K_PLANAR, oracle.TYPE_Q5_K, synth.q5_k_weights),
 }
 
 
@@ -31,6 +32,8 @@ def _weights(kind, rows, K, salt):
         Wd = mmvq.repack_planar(Wd, rows, K)
     if kind == "q4_k_planar":
         Wd = mmvq.repack_planar(Wd, rows, K, type_=mmvq.TYPE_Q4_K)
+    if kind == "q5_k_planar":
+        Wd = mmvq.repack_planar(Wd, rows, K, type_=mmvq.TYPE_Q5_K)
     return W, Wd, t_gpu, t_orc
 
 

@@ -63,6 +63,17 @@ def test_q4_k_dense_shapes(rows, K, planar):
         _check_sampled(t, oracle.TYPE_Q4_K, W, Wd, rows, K, x, ncols, salt=ncols)
 
 
+@pytest.mark.parametrize("rows,K", [(12288, 2560), (6144, 2560), (2560, 6144), (640, 2560),
+                                    (512, 2560)])
+def test_q5_k_dense_shapes(rows, K):
+    W = synth.q5_k_weights(rows, K, salt=rows + K)
+    Wd = mmvq.repack_planar(dev(W), rows, K, type_=mmvq.TYPE_Q5_K)
+    for ncols in (1, 4):
+        x = synth.activations(K, ncols, salt=ncols)
+        _check_sampled(mmvq.TYPE_Q5_K_PLANAR, oracle.TYPE_Q5_K, W, Wd, rows, K, x, ncols,
+                       salt=ncols)
+
+
 def test_lm_head_and_draft_head():
     rows, K = 151936, 2560
     W = synth.q6_k_weights(rows, K, salt=7)

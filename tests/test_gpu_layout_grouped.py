@@ -30,6 +30,13 @@ def test_repack_q4_bit_exact(rows, K):
     assert np.array_equal(got, oracle.repack_planar(W, rows, K, oracle.TYPE_Q4_K))
 
 
+@pytest.mark.parametrize("rows,K", [(1, 256), (16, 256), (37, 512), (300, 2560), (45, 10240)])
+def test_repack_q5_bit_exact(rows, K):
+    W = synth.q5_k_weights(rows, K, salt=rows + K)
+    got = host(mmvq.repack_planar(dev(W), rows, K, type_=mmvq.TYPE_Q5_K))
+    assert np.array_equal(got, oracle.repack_planar(W, rows, K, oracle.TYPE_Q5_K))
+
+
 @pytest.mark.parametrize("rows,K,n", [(300, 512, 37), (1000, 2560, 64), (40, 256, 1)])
 def test_gather_bit_exact(rows, K, n):
     W = synth.q6_k_weights(rows, K, salt=n)
