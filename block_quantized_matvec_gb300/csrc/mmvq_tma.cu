@@ -877,7 +877,21 @@ static int grouped_config(int64_t rows, int K, int64_t est_active, GroupedCfg* o
       break;
     }
   if (G == 0) G = std::max(1, std::min(4, 12 / P));
-  while (S > 2 && grouped_smem_bytes(LAYOUT, S, K, CM, G, P) > limit) --S;
+  // long rows with 8-position chunks: fewer stages, then fewer row groups
+  // and K-slices per stage, until the ring fits beside the activations
+  while (grouped_smem_bytes(LAYOUT, S, K, CM, G, P) > limit) {
+    if (S > 2) {
+      --S;
+    } else if (G > 1) {
+      --G;
+    } else if (P > 1) {
+      int d = P - 1;
+      while (d > 1 && nb % d) --d;
+      P = d;
+    } else {
+      break;
+    }
+  }
   const size_t smem = grouped_smem_bytes(LAYOUT, S, K, CM, G, P);
   if (smem > limit) return MMVQ_ERR_SHAPE;
   if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;

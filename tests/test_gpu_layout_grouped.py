@@ -143,6 +143,15 @@ _KIND_TYPE = {"q4_k": mmvq.TYPE_Q4_K, "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR,
               "q6_k_planar": mmvq.TYPE_Q6_K_PLANAR}
 
 
+@pytest.mark.parametrize("kind", ["q4_k_planar", "q6_k_planar"])
+def test_grouped_longest_rows_with_full_position_chunks(kind):
+    # K = 16384 with groups of about 10 positions (chunks of 8): the launch
+    # shape must still fit its ring beside eight staged activation columns
+    y, y_ref, bound, st = _grouped_case(kind, 20, 2, 4, 48, 16384, salt=6)
+    assert st == 0
+    assert_within_bound(y, y_ref, bound, f"{kind} K=16384")
+
+
 @pytest.mark.parametrize("kind", ["q4_k", "q4_k_planar", "q6_k_planar"])
 def test_grouped_all_groups_empty_writes_nothing(kind):
     E, rows, K = 8, 32, 256
