@@ -83,12 +83,14 @@ WORKLOAD_DESC = {
 }
 
 
-MMVQ_SOURCES = ["api.cu", "common.cuh", "kquant.cuh", "mmvq_dense.cu", "mmvq_tma.cu", "rowgroup.cuh"]
+MMVQ_SOURCES = ["api.cu", "common.cuh", "expert_ffn.cuh", "ffn_args.cuh", "kquant.cuh", "mmvq_dense.cu",
+                "mmvq_tma.cu", "q8_1.cuh", "route.cuh", "rowgroup.cuh"]
 
 
 def kernel_source_hash() -> str:
-    """sha256 of the sources the profiled MMVQ kernels (dense ring, grouped
-    ring, their launch choosers) are built from, and of the ABI header."""
+    """sha256 of the sources the profiled kernels (dense ring, grouped ring,
+    the one-launch expert layer, their launch choosers) are built from, and
+    of the ABI header."""
     import hashlib
     h = hashlib.sha256()
     for p in [os.path.join(HERE, "block_quantized_matvec_gb300", "csrc", f) for f in MMVQ_SOURCES] + \
@@ -478,13 +480,17 @@ def run_ours(args, rank, world, local_rank):
 # ------------------------------------------------------------- MoE step --
 
 def run_moe(args, rank, world, local_rank):
-    """One step = the routed-expert hot path for T tokens: Q8_1 quantise the
-    hidden states and build the per-expert token lists from the top-k routing
-    (one launch), grouped gate|up MMVQ, SiLU(gate)*up requantised to Q8_1,
-    grouped down MMVQ.
-    Experts are planar Q4_K tiles; each step uses the next of 16 seeded
-    routings, so consecutive steps read different experts.  Weight bytes =
-    distinct experts read x (gate|up + down) bytes."""
+    """One step = the routed-expert FFN of one MoE layer for T tokens in one
+    launch (mmvq_expert_ffn): the per-expert token lists from the top-k
+    routing, Q8_1 of the hidden states, grouped gate|up MMVQ, SiLU(gate)*up
+    requantised to Q8_1, grouped down MMVQ.  The same step as the four
+    separate launches (quantise + route, grouped gate|up, SiLU*up -> Q8_1,
+    grouped down) is timed beside it as `chain`.
+    Experts are planar Q4_K tiles; step i uses routing i mod 16, so
+    consecutive steps read different experts (the 16 routings together touch
+    far more expert bytes than L2 holds).  Each timed region is one CUDA graph
+    of exactly K steps.  Weight bytes = distinct experts read x (gate|up +
+    down) bytes."""
     import torch
     from block_quantized_matvec_gb300 import metrics, mmvq, synth
 
@@ -502,87 +508,111 @@ def run_moe(args, rank, world, local_rank):
         for e in range(E):
             mmvq.repack_planar(torch.from_numpy(host[e].reshape(-1)).to(dev), rows, K,
                                out=out[e * per:(e + 1) * per], type_=q4)
-        return host, out
+        return out
 
-    gu_host, W_gu = planar_experts(2 * F, H, 1)
-    dn_host, W_dn = planar_experts(H, F, 2)
+    W_gu = planar_experts(2 * F, H, 1)
+    W_dn = planar_experts(H, F, 2)
     R = 16
     topks = [synth.routing(T, k, E, salt=100 + r) for r in range(R)]
     topk_dev = [torch.from_numpy(t).to(dev) for t in topks]
-    x_host = synth.activations(H, T)
+    x_host = synth.moe_hidden(H, T)
     x_dev = torch.from_numpy(x_host).to(dev)
     x_pinned = torch.from_numpy(x_host).pin_memory()
+    topk_pinned = torch.from_numpy(topks[0]).pin_memory()
+    topk_e2e = torch.empty_like(topk_dev[0])
     n = T * k
     xq = torch.empty((T, H // 32, 36), dtype=torch.uint8, device=dev)
     gu = torch.empty((n, 2 * F), device=dev)
     hq = torch.empty((n, F // 32, 36), dtype=torch.uint8, device=dev)
     y = torch.empty((n, H), device=dev)
     y_pinned = torch.empty((n, H)).pin_memory()
-    torch.cuda.synchronize()
+    lists = dict(expert_ids=torch.empty(E, dtype=torch.int32, device=dev),
+                 offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                 act_index=torch.empty(n, dtype=torch.int32, device=dev),
+                 slot_of=torch.empty(n, dtype=torch.int32, device=dev))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sync = mmvq.expert_ffn_workspace(dev)
 
-    def step(r, s=None, evs=None):
+    def fused(topk):
+        # the layer in one launch (token lists written for a later combine)
+        mmvq.lib().mmvq_expert_ffn(
+            mmvq.TYPE_Q4_K_PLANAR, W_gu.data_ptr(), W_dn.data_ptr(), E, H, F, x_dev.data_ptr(), H,
+            T, topk.data_ptr(), k, gu.data_ptr(), hq.data_ptr(), y.data_ptr(),
+            lists["expert_ids"].data_ptr(), lists["offsets"].data_ptr(),
+            lists["act_index"].data_ptr(), lists["slot_of"].data_ptr(), xq.data_ptr(),
+            status.data_ptr(), sync.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+    def chain(topk, evs=None, s=None):
         rec = (lambda i: _record_external(evs[i], s)) if evs is not None else (lambda i: None)
         rec(0)
-        # hidden-state Q8_1 and the per-expert lists in one launch
-        _, eids, offs, act, _, status = mmvq.quantize_route_groups(x_dev, topk_dev[r], E, xq=xq)
+        _, eids, offs, act, _, st = mmvq.quantize_route_groups(x_dev, topk, E, xq=xq)
         rec(1)
         mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_gu, E, 2 * F, H, eids, offs, act, xq, T, n, out=gu,
-                     status=status)
+                     status=st)
         rec(2)
         mmvq.silu_mul_quantize_q8_1(gu, F, out=hq)
         rec(3)
         mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_dn, E, H, F, eids, offs, None, hq, n, n, out=y,
-                     status=status)
+                     status=st)
         rec(4)
 
+    def capture(fn, n_steps, first=0):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+            for i in range(n_steps):
+                fn(topk_dev[(first + i) % R])
+        torch.cuda.synchronize()
+        return g
+
     for r in range(R):
-        step(r)
+        fused(topk_dev[r])
+        chain(topk_dev[r])
     torch.cuda.synchronize()
-    # timed graphs: the five kernels back to back (each may start while its
-    # predecessor drains); breakdown graphs: the same with an event node
-    # between kernels, replayed after the timed region
-    graphs, graphs_ev, events = [], [], []
+    if int(status.item()) != 0 or mmvq.read_device_fault() != 0:
+        raise RuntimeError("expert FFN reported a routing error or a device fault")
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    clocks.wait_first_sample()
+    timed = {}
+    stream = torch.cuda.current_stream()
+    for name, fn in (("fused", fused), ("chain", chain)):
+        warm = capture(fn, max(3, args.warmup), first=R - 1)
+        g = capture(fn, args.steps)
+        warm.replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        if name == "fused":
+            clocks.mark()
+        t0.record(stream)
+        g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        timed[name] = max_over_ranks(t0.elapsed_time(t1), world, dev)
+        barrier(world)
+        del g, warm
+    clk = clocks.stop()
+
+    # the chain's kernels one by one: a graph per routing with event nodes
+    # between the four launches, replayed after the timed regions
+    dur_runs = []
     for r in range(R):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         for e in evs:
             e.record()
         torch.cuda.synchronize()
-        for with_ev in (False, True):
-            g = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream(device=dev)
-            cap.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
-                step(r, torch.cuda.current_stream(), evs if with_ev else None)
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+            chain(topk_dev[r], evs, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        for rep in range(4):
+            g.replay()
             torch.cuda.synchronize()
-            (graphs_ev if with_ev else graphs).append(g)
-        events.append(evs)
-
-    stream = torch.cuda.current_stream()
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    for i in range(args.warmup):
-        graphs[i % R].replay()
-    torch.cuda.synchronize()
-    clocks.wait_first_sample()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    clocks.mark()
-    t0.record(stream)
-    for i in range(args.steps):
-        graphs[i % R].replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    barrier(world)
-
-    dur_runs = []
-    for rep in range(4):
-        for r in range(R):
-            graphs_ev[r].replay()
-            torch.cuda.synchronize()
-            evs = events[r]
             dur_runs.append([evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(4)])
 
     distinct = [len(np.unique(t)) for t in topks]
@@ -593,46 +623,61 @@ def run_moe(args, rank, world, local_rank):
     gu_bytes = np.mean([d * metrics.weight_bytes("q4_k", 2 * F, H) for d in distinct])
     dn_bytes = np.mean([d * metrics.weight_bytes("q4_k", H, F) for d in distinct])
     peak, peak_kind = load_peak()
-    achieved = gu_bytes / (mean_us[1] * 1e-6) / 1e9
-    # DRAM bytes per gate|up launch: the profiled traffic / weight-byte ratio
-    # (T=8 capture) applied to this run's mean weight bytes per launch
-    ratio = profiled_field("mmvq_grouped_moe_t8.md", "traffic_over_weight_bytes_gate_up")
-    gu_traffic = None if ratio is None else round(ratio * gu_bytes)
+    fused_ms = timed["fused"]
+    # the fused kernel is the whole step: its algorithmic bytes per launch are
+    # the step's weight bytes plus the activations it reads and writes
+    act_bytes = T * H * 4 + T * (H // 32) * 36 + n * (2 * F * 4 * 2 + (F // 32) * 36 * 2 + H * 4)
+    launch_bytes = float(np.mean(step_bytes)) + act_bytes
+    achieved = launch_bytes / (fused_ms * 1e-3 / args.steps) / 1e9
+    # DRAM bytes per launch: the profiled traffic / weight-byte ratio (T=8
+    # capture) applied to this run's mean weight bytes
+    ratio = profiled_field("mmvq_expert_ffn_moe_t8.md", "traffic_over_weight_bytes")
+    traffic = None if ratio is None else round(ratio * float(np.mean(step_bytes)))
 
     e2e_steps = max(3, min(args.steps, 200))
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     for i in range(e2e_steps):
         x_dev.copy_(x_pinned, non_blocking=True)
-        graphs[i % R].replay()
+        topk_e2e.copy_(topk_pinned, non_blocking=True)
+        mmvq.expert_ffn(mmvq.TYPE_Q4_K_PLANAR, W_gu, W_dn, E, H, F, x_dev, topk_e2e, gu=gu, hq=hq,
+                        y=y, xq=xq, sync=sync, lists=False)
         y_pinned.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - w0) / e2e_steps, world, dev)
+    if mmvq.read_device_fault() != 0:
+        raise RuntimeError("device fault word set after the timed runs")
+    e2e_bytes = metrics.moe_step_bytes(distinct[0], H, F)
 
     out = {
-        "metric": METRIC, "value": round(world * total_bytes / (elapsed_ms * 1e-3) / 1e9, 1),
+        "metric": METRIC, "value": round(world * total_bytes / (fused_ms * 1e-3) / 1e9, 1),
         "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "ms_per_step": round(fused_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a + fp32",
         "data": "synthetic (seeded generators shaped like the pages' matrices)",
         "config": {"workload": WORKLOAD_DESC[args.workload], "tokens": T, "routings": R,
                    "parallelism": f"replicas x{world}",
                    "distinct_experts_mean": float(np.mean(distinct)),
-                   "timing": "CUDA graph replay of whole steps; per-kernel times from a "
-                             "second graph with event nodes between the five kernels"},
+                   "l2": "inputs larger than L2: 16 routings cycled, their experts far exceed L2",
+                   "timing": "one CUDA graph of exactly `steps` steps per path"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 3), "traffic": gu_traffic,
-                     "algorithmic_bytes_per_launch": round(gu_bytes),
-                     "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "grouped gate|up MMVQ"},
-        "e2e": {"value": round(world * np.mean(step_bytes) / e2e_s / 1e9, 1), "unit": UNIT,
-                "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y.numel() * 4),
-                "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
+                     "frac": round(achieved / peak, 3), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": round(launch_bytes),
+                     "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "mmvq_expert_ffn_kernel"},
+        "e2e": {"value": round(world * e2e_bytes / e2e_s / 1e9, 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_host.nbytes + topks[0].nbytes),
+                "d2h_bytes_per_step": int(y.numel() * 4), "steps": e2e_steps,
+                "call": "mmvq.expert_ffn, routing 0 every step"},
+        "gpu_launches": args.steps,
         "clocks": clk,
-        "kernels_us": {nm: round(float(v), 3) for nm, v in zip(names, mean_us)},
-        "grouped_gbps": {"gate_up": round(gu_bytes / mean_us[1] / 1e3, 1),
-                         "down": round(dn_bytes / mean_us[3] / 1e3, 1)},
+        "chain": {"ms_per_step": round(timed["chain"] / args.steps, 4),
+                  "value": round(world * total_bytes / (timed["chain"] * 1e-3) / 1e9, 1),
+                  "launches_per_step": 4,
+                  "kernels_us": {nm: round(float(v), 3) for nm, v in zip(names, mean_us)},
+                  "grouped_gbps": {"gate_up": round(gu_bytes / mean_us[1] / 1e3, 1),
+                                   "down": round(dn_bytes / mean_us[3] / 1e3, 1)},
+                  "note": "kernels_us from a graph with event nodes between the launches"},
     }
     return out
 

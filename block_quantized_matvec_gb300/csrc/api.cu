@@ -4,6 +4,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "ffn_args.cuh"
 
 namespace mmvq {
 int launch_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, void* xq, cudaStream_t s);
@@ -161,6 +162,74 @@ int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, i
                               n_groups, act_index, xq, n_xq_cols, y, status, (cudaStream_t)stream);
 }
 
+static int check_expert_ffn(int type, const void* W_gate_up, const void* W_down, int n_experts,
+                            int H, int F, const float* x, int64_t ldx, int T, const int32_t* topk,
+                            int k) {
+  if (type != MMVQ_Q4_K_PLANAR && type != MMVQ_Q6_K_PLANAR) return MMVQ_ERR_TYPE;
+  if (!W_gate_up || !W_down || !x || !topk) return MMVQ_ERR_NULL;
+  if (H < mmvq::kQK || H > mmvq::kMaxK || H % mmvq::kQK != 0 || F < mmvq::kQK ||
+      F > mmvq::kMaxK || F % mmvq::kQK != 0 || ldx < H)
+    return MMVQ_ERR_SHAPE;
+  if (T < 1 || T > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
+  if (k < 1 || k > 256 || T * k > 256) return MMVQ_ERR_SHAPE;
+  if (n_experts < 1 || n_experts > 1024) return MMVQ_ERR_ROUTING;
+  return MMVQ_OK;
+}
+
+int mmvq_expert_ffn(int type, const void* W_gate_up, const void* W_down, int n_experts, int H,
+                    int F, const float* x, int64_t ldx, int T, const int32_t* topk, int k,
+                    float* gu, void* hq, float* y, int32_t* expert_ids, int32_t* token_offsets,
+                    int32_t* act_index, int32_t* slot_of, void* xq, int32_t* status,
+                    uint32_t* sync, mmvq_stream_t stream) {
+  int rc = check_expert_ffn(type, W_gate_up, W_down, n_experts, H, F, x, ldx, T, topk, k);
+  if (rc) return rc;
+  if (!gu || !hq || !y || !xq || !sync) return MMVQ_ERR_NULL;
+  if (!aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(hq, 16) || !aligned(xq, 16) || !aligned(x, 4) || !aligned(topk, 4) || !aligned(gu, 4) ||
+      !aligned(y, 4) || !aligned(sync, 4) || (expert_ids && !aligned(expert_ids, 4)) ||
+      (token_offsets && !aligned(token_offsets, 4)) || (act_index && !aligned(act_index, 4)) ||
+      (slot_of && !aligned(slot_of, 4)) || (status && !aligned(status, 4)))
+    return MMVQ_ERR_ALIGN;
+  mmvq::FfnArgs a = {};
+  a.w_gu = static_cast<const uint8_t*>(W_gate_up);
+  a.w_dn = static_cast<const uint8_t*>(W_down);
+  a.n_experts = n_experts;
+  a.H = H;
+  a.F = F;
+  a.x = x;
+  a.ldx = ldx;
+  a.T = T;
+  a.topk = topk;
+  a.k = k;
+  a.gu = gu;
+  a.hq = static_cast<uint8_t*>(hq);
+  a.y = y;
+  a.expert_ids = expert_ids;
+  a.offsets = token_offsets;
+  a.act_index = act_index;
+  a.slot_of = slot_of;
+  a.xq = static_cast<uint8_t*>(xq);
+  a.status = status;
+  a.sync = sync;
+  return mmvq::launch_expert_ffn(type, a, (cudaStream_t)stream, nullptr);
+}
+
+int mmvq_expert_ffn_shape(int type, int n_experts, int H, int F, int T, int k, int32_t* info) {
+  // any non-null, aligned pointers: only the shape rules are checked here
+  static const uint64_t dummy[2] = {0, 0};
+  int rc = check_expert_ffn(type, dummy, dummy, n_experts, H, F,
+                            reinterpret_cast<const float*>(dummy), H, T,
+                            reinterpret_cast<const int32_t*>(dummy), k);
+  if (rc) return rc;
+  if (!info) return MMVQ_ERR_NULL;
+  mmvq::FfnArgs a = {};
+  a.n_experts = n_experts;
+  a.H = H;
+  a.F = F;
+  a.T = T;
+  a.k = k;
+  return mmvq::launch_expert_ffn(type, a, nullptr, info);
+}
+
 int mmvq_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
                       int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
                       int32_t* status, mmvq_stream_t stream) {
@@ -225,6 +294,14 @@ int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
 int mmvq_selftest_wait_timeout(unsigned int limit_us, mmvq_stream_t stream) {
   if (limit_us < 1 || limit_us > 100000) return MMVQ_ERR_SHAPE;
   return mmvq::launch_wait_timeout_selftest(limit_us, (cudaStream_t)stream);
+}
+
+int mmvq_selftest_grid_barrier_timeout(uint32_t* sync, unsigned int limit_us,
+                                       mmvq_stream_t stream) {
+  if (!sync) return MMVQ_ERR_NULL;
+  if (!aligned(sync, 4)) return MMVQ_ERR_ALIGN;
+  if (limit_us < 1 || limit_us > 100000) return MMVQ_ERR_SHAPE;
+  return mmvq::launch_grid_barrier_selftest(sync, limit_us, (cudaStream_t)stream);
 }
 
 int mmvq_rmsnorm_quantize_q8_1(const float* x, const float* w, float eps, int K, int ncols,

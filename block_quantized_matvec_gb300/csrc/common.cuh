@@ -83,8 +83,10 @@ __device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
 // da/sa: [ncols][K/32].  col_of(c) gives the xq column for local column c,
 // or -1 for a column to stage as zeros.  A column's blocks are one
 // contiguous, 16-byte aligned run of 36*K/32 bytes (K % 256 == 0), read
-// here 16 bytes per thread and scattered word by word.
-template <typename ColOf>
+// here 16 bytes per thread and scattered word by word.  kCoherent reads
+// through L2 only (ld.global.cg), for columns written earlier in the same
+// launch by other CTAs; otherwise the read-only path.
+template <bool kCoherent = false, typename ColOf>
 __device__ __forceinline__ void stage_q8_1(const uint8_t* __restrict__ xq, int K, int ncols,
                                            ColOf col_of, uint8_t* act, float* da, float* sa,
                                            int tid, int nthreads) {
@@ -96,7 +98,10 @@ __device__ __forceinline__ void stage_q8_1(const uint8_t* __restrict__ xq, int K
     const int col = col_of(c);
     uint4 q = make_uint4(0u, 0u, 0u, 0u);
     if (col >= 0)
-      q = __ldg(reinterpret_cast<const uint4*>(xq + (size_t)col * nbq * kQ81Bytes) + vi);
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)col * nbq * kQ81Bytes) + vi;
+      q = kCoherent ? __ldcg(src) : __ldg(src);
+    }
     const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {

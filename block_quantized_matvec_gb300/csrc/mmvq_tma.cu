@@ -996,3 +996,7 @@ int read_device_fault(int* fault, cudaStream_t stream) {
 }
 
 }  // namespace mmvq
+
+// The one-launch expert FFN shares this translation unit's ring routines
+// and device fault word.
+#include "expert_ffn.cuh"

@@ -1,48 +1,10 @@
-// Q8_1 activation quantisation and the SiLU(gate)*up requantisation.
-//
-// Q8_1 ("Strata" PR #2340 "int4 activation loads"; PR #1774 "d * ds *
-// sumi"): per 32 values, amax, d = amax/127, q = round-half-away(x/d),
-// s = d*sum(q); d and s stored as fp16 (round to nearest even).  One warp
-// per block, one value per lane; IEEE division and roundf (no fast-math),
-// so the bytes are exactly those of the plain definition.
+// Q8_1 activation quantisation and the SiLU(gate)*up requantisation: one
+// warp per 32-value block, the arithmetic of q8_1.cuh.
 #include "common.cuh"
+#include "q8_1.cuh"
 #include "route.cuh"
 
 namespace mmvq {
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// One lane's value v of a 32-value block -> writes the 36-byte block at out.
-__device__ __forceinline__ void quantize_lane(float v, uint8_t* out, int lane) {
-  const float amax = warp_max(fabsf(v));
-  const float d = __fdiv_rn(amax, 127.0f);
-  const int q = (d != 0.0f) ? (int)roundf(__fdiv_rn(v, d)) : 0;
-  const int sum = warp_sum(q);
-  // Pack four quants per lane 0..7 so the block is written with word stores.
-  const uint32_t b = (uint32_t)(q & 0xff);
-  const uint32_t b1 = __shfl_down_sync(0xffffffffu, b, 1);
-  const uint32_t b2 = __shfl_down_sync(0xffffffffu, b, 2);
-  const uint32_t b3 = __shfl_down_sync(0xffffffffu, b, 3);
-  const uint32_t word = b | (b1 << 8) | (b2 << 16) | (b3 << 24);
-  uint32_t* o32 = reinterpret_cast<uint32_t*>(out);
-  if ((lane & 3) == 0) o32[1 + (lane >> 2)] = word;
-  if (lane == 0) {
-    const float s = __fmul_rn(d, (float)sum);
-    const uint32_t hd = __half_as_ushort(__float2half_rn(d));
-    const uint32_t hs = __half_as_ushort(__float2half_rn(s));
-    o32[0] = hd | (hs << 16);
-  }
-}
 
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int K,
                                                             int ncols, int64_t ldx,
@@ -73,10 +35,7 @@ __global__ void __launch_bounds__(256) silu_mul_quantize_kernel(const float* __r
   const int r = (int)(blk / nbq);
   const int kb = (int)(blk - (int64_t)r * nbq);
   const float* row = gu + (int64_t)r * 2 * F;
-  const float g = row[kb * kQK8 + lane];
-  const float u = row[F + kb * kQK8 + lane];
-  const float sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-  const float h = __fmul_rn(sg, u);
+  const float h = silu_mul(row[kb * kQK8 + lane], row[F + kb * kQK8 + lane]);
   if (h_out) h_out[(int64_t)r * F + kb * kQK8 + lane] = h;
   quantize_lane(h, xq + blk * kQ81Bytes, lane);
 }

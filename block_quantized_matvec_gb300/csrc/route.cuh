@@ -1,13 +1,17 @@
 // Per-expert token lists: the routing step of the grouped expert calls
 // ("Strata" PR #2746 "B70 validation": per-expert token groups, empty groups
 // allowed), as the work of one CTA: counting sort of the routing slots by
-// expert, stable in slot order.  Slot s = t*k + j.  The CTA's threads own
-// four experts each (blockDim.x >= n_experts / 4).
+// expert, stable in slot order.  Slot s = t*k + j.  Thread t owns the
+// ceil(n_experts / blockDim.x) consecutive experts from t times that count
+// (n_experts <= kMaxE, blockDim.x a multiple of 32, at most 1024).  The
+// outputs may live in global or shared memory; expert_ids and status may be
+// NULL.
 #pragma once
 #include "common.cuh"
 
 namespace mmvq {
 
+template <int kMaxE = 4096>
 __device__ __forceinline__ void route_groups_cta(const int32_t* __restrict__ topk, int n_slots,
                                                  int k, int n_experts,
                                                  int32_t* __restrict__ expert_ids,
@@ -15,7 +19,7 @@ __device__ __forceinline__ void route_groups_cta(const int32_t* __restrict__ top
                                                  int32_t* __restrict__ act_index,
                                                  int32_t* __restrict__ slot_of,
                                                  int32_t* __restrict__ status) {
-  __shared__ int cnt[4096];
+  __shared__ int cnt[kMaxE];
   __shared__ int wsum[33];
   const int tid = threadIdx.x;
   for (int e = tid; e < n_experts; e += blockDim.x) cnt[e] = 0;
@@ -29,15 +33,11 @@ __device__ __forceinline__ void route_groups_cta(const int32_t* __restrict__ top
     }
   }
   __syncthreads();
-  // exclusive scan: thread tid owns experts [4tid, 4tid+4)
-  int local[4];
+  // exclusive scan over the experts, each thread's run of them in order
+  const int per = (n_experts + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int e_lo = min(n_experts, tid * per), e_hi = min(n_experts, e_lo + per);
   int sum = 0;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = 4 * tid + u;
-    local[u] = e < n_experts ? cnt[e] : 0;
-    sum += local[u];
-  }
+  for (int e = e_lo; e < e_hi; ++e) sum += cnt[e];
   const int lane = tid & 31, warp = tid >> 5;
   int x = sum;
 #pragma unroll
@@ -61,15 +61,12 @@ __device__ __forceinline__ void route_groups_cta(const int32_t* __restrict__ top
   }
   __syncthreads();
   int run = wsum[warp] + x - sum;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = 4 * tid + u;
-    if (e < n_experts) {
-      offsets[e] = run;
-      expert_ids[e] = e;
-      cnt[e] = run;  // becomes the placement cursor
-    }
-    run += local[u];
+  for (int e = e_lo; e < e_hi; ++e) {
+    const int c = cnt[e];
+    offsets[e] = run;
+    if (expert_ids) expert_ids[e] = e;
+    cnt[e] = run;  // becomes the placement cursor
+    run += c;
   }
   if (tid == 0) offsets[n_experts] = wsum[32];
   __syncthreads();

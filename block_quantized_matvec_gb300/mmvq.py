@@ -51,6 +51,10 @@ SIGNATURES = {
     "mmvq_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "mmvq_rmsnorm_quantize_q8_1": (_I, [_P, _P, ctypes.c_float, _I, _I, _I64, _P, _P, _P]),
     "mmvq_launch_shape": (_I, [_I, _I64, _I, _I, _P]),
+    "mmvq_expert_ffn": (_I, [_I, _P, _P, _I, _I, _I, _P, _I64, _I, _P, _I, _P, _P, _P, _P, _P,
+                             _P, _P, _P, _P, _P, _P]),
+    "mmvq_expert_ffn_shape": (_I, [_I, _I, _I, _I, _I, _I, _P]),
+    "mmvq_selftest_grid_barrier_timeout": (_I, [_P, ctypes.c_uint, _P]),
 }
 
 
@@ -194,6 +198,72 @@ def quantize_route_groups(x: torch.Tensor, topk: torch.Tensor, n_experts: int,
                                             _ptr(status), _stream(stream)),
            "mmvq_quantize_route_groups")
     return xq, eids, offs, act, slot, status
+
+
+def expert_ffn_workspace(device) -> torch.Tensor:
+    """A zeroed grid-barrier word for expert_ffn (one per concurrently running launch)."""
+    return torch.zeros(4, dtype=torch.int32, device=device)
+
+
+def expert_ffn(type_: int, W_gate_up: torch.Tensor, W_down: torch.Tensor, n_experts: int,
+               H: int, F: int, x: torch.Tensor, topk: torch.Tensor, *,
+               gu: torch.Tensor | None = None, hq: torch.Tensor | None = None,
+               y: torch.Tensor | None = None, lists: bool = True, xq: torch.Tensor | None = None,
+               status: torch.Tensor | None = None, sync: torch.Tensor | None = None,
+               stream=None) -> dict:
+    """The routed-expert FFN of one MoE layer in one launch: x [T, H] fp32 (T <= 8),
+    topk [T, k] int32, planar experts W_gate_up (2F x H each) and W_down (H x F
+    each).  Returns a dict with xq [T, H/32, 36], gu [T*k, 2F], hq [T*k, F/32, 36],
+    y [T*k, H] and, with lists=True, expert_ids, offsets, act_index, slot_of."""
+    for t, n in ((W_gate_up, "W_gate_up"), (W_down, "W_down"), (x, "x"), (topk, "topk")):
+        _dev(t, n)
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    T, k = topk.shape
+    n = T * k
+    dev = x.device
+    if gu is None:
+        gu = torch.empty((n, 2 * F), dtype=torch.float32, device=dev)
+    if hq is None:
+        hq = torch.empty((n, F // 32, Q8_1_BYTES), dtype=torch.uint8, device=dev)
+    if y is None:
+        y = torch.empty((n, H), dtype=torch.float32, device=dev)
+    out = {"gu": gu, "hq": hq, "y": y}
+    if lists:
+        out.update(expert_ids=torch.empty(n_experts, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(n_experts + 1, dtype=torch.int32, device=dev),
+                   act_index=torch.empty(max(n, 1), dtype=torch.int32, device=dev),
+                   slot_of=torch.empty(max(n, 1), dtype=torch.int32, device=dev))
+    if xq is None:
+        xq = torch.empty((T, H // 32, Q8_1_BYTES), dtype=torch.uint8, device=dev)
+    out["xq"] = xq
+    if status is not None:
+        out["status"] = status
+    if sync is None:
+        sync = expert_ffn_workspace(dev)
+    _check(lib().mmvq_expert_ffn(type_, _ptr(W_gate_up), _ptr(W_down), n_experts, H, F, _ptr(x),
+                                 x.stride(0), T, _ptr(topk), k, _ptr(gu), _ptr(hq), _ptr(y),
+                                 _ptr(out.get("expert_ids")), _ptr(out.get("offsets")),
+                                 _ptr(out.get("act_index")), _ptr(out.get("slot_of")),
+                                 _ptr(xq), _ptr(status), _ptr(sync), _stream(stream)),
+           "mmvq_expert_ffn")
+    return out
+
+
+def expert_ffn_shape(type_: int, n_experts: int, H: int, F: int, T: int, k: int) -> dict:
+    """The launch shape mmvq_expert_ffn picks (host-only)."""
+    info = (ctypes.c_int32 * 8)()
+    _check(lib().mmvq_expert_ffn_shape(type_, n_experts, H, F, T, k, info),
+           "mmvq_expert_ffn_shape")
+    keys = ("grid", "threads", "smem", "stages", "G_gate_up", "P_gate_up", "G_down", "P_down")
+    return dict(zip(keys, list(info)))
+
+
+def selftest_grid_barrier_timeout(sync: torch.Tensor, limit_us: int = 2000, stream=None) -> None:
+    """Run the expert FFN's grid barrier to expiry on its own word (sets bit 2 of the fault word)."""
+    _dev(sync, "sync")
+    _check(lib().mmvq_selftest_grid_barrier_timeout(_ptr(sync), limit_us, _stream(stream)),
+           "mmvq_selftest_grid_barrier_timeout")
 
 
 def route_groups(topk: torch.Tensor, n_experts: int, stream=None):

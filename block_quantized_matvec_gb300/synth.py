@@ -107,6 +107,14 @@ def activations(K: int, ncols: int, salt: int = 0, seed: int = SEED_ACTIVATIONS)
     return rng.standard_normal(size=(ncols, K), dtype=np.float32)
 
 
+def moe_hidden(H: int, T: int, salt: int = 0, seed: int = SEED_ACTIVATIONS) -> np.ndarray:
+    """Hidden states entering an expert layer, ``[T, H]``: N(0, 1) scaled by 2^-6
+    (exact), so that with the synthetic expert weights (whose values run a
+    hundred times larger than trained ones) SiLU(gate)*up stays well inside
+    the fp16 range of the Q8_1 scale and sum fields."""
+    return activations(H, T, salt=salt, seed=seed) * np.float32(1.0 / 64.0)
+
+
 def routing(T: int, k: int = 8, n_experts: int = 256, salt: int = 0,
             seed: int = SEED_ROUTING) -> np.ndarray:
     """Top-k expert ids per token, ``[T, k]`` int32, distinct within a token."""

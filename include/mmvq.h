@@ -3,9 +3,9 @@
  * matrix-vector products (MMVQ) at 1-8 columns, for NVIDIA GB300 (sm_103a).
  *
  * Conventions for every entry point:
- *  - Pointers named W, xq, x, y, gu, sumi, row_ids, topk, expert_ids,
- *    token_offsets, act_index, status and out are DEVICE pointers, owned by
- *    the caller, who allocates and frees them.  The library allocates no
+ *  - Pointers named W (W_*), xq, hq, x, y, gu, sumi, row_ids, topk,
+ *    expert_ids, token_offsets, act_index, slot_of, status, sync and out are
+ *    DEVICE pointers, owned by the caller, who allocates and frees them.  The library allocates no
  *    device or host memory and never synchronises the stream.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream).  Launch failures are reported by the return
@@ -232,6 +232,61 @@ MMVQ_API int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq
                                 mmvq_stream_t stream);
 
 /*
+ * The routed-expert FFN of one MoE layer in one launch (issue #2801: the
+ * grouped gate/up and down kernels with the activation between them; PR
+ * #2746: grouped calls over per-expert token groups).  For T tokens (1..8)
+ * routed to k experts each by topk (int32 [T][k]) it computes:
+ *  - the token lists of mmvq_route_groups (position p runs over the valid
+ *    routing entries in expert order, tokens in order inside an expert);
+ *  - gu[p][0..2F) = the gate|up matrix of expert e(p) (W_gate_up: n_experts
+ *    planar matrices of 2F x H, one after another, gate rows first) times
+ *    Q8_1(x[token(p)]), as mmvq_grouped;
+ *  - hq[p] = Q8_1(SiLU(gate) * up) as mmvq_silu_mul_quantize_q8_1;
+ *  - y[p][0..H) = the down matrix of expert e(p) (W_down: n_experts planar
+ *    matrices of H x F) times hq[p], as mmvq_grouped.
+ * Each step uses the arithmetic of its separate entry point: Q8_1 bytes and
+ * per-32-block integer sums are the same, fp32 sums may be added in another
+ * order.
+ *   type: MMVQ_Q4_K_PLANAR or MMVQ_Q6_K_PLANAR (both matrices).
+ *   x: fp32 [T][ldx], ldx >= H.  xq: Q8_1 [T][H/32], the quantised hidden
+ *   states (written, then read by the gate|up step).  gu: fp32 [T*k][2F];
+ *   hq: Q8_1 [T*k][F/32]; y: fp32 [T*k][H]; rows p >= the number of valid
+ *   entries are not written.  expert_ids [n_experts], token_offsets
+ *   [n_experts+1], act_index [T*k] and slot_of [T*k] are optional outputs
+ *   (NULL: not written) holding what mmvq_quantize_route_groups gives.
+ *   status (optional): set to MMVQ_ERR_ROUTING when an expert id lies
+ *   outside [0, n_experts) (that entry is dropped).
+ *   sync: one uint32 word, zero before the first call.  The launch uses it
+ *   as its grid-barrier counter and leaves its low 31 bits zero (the top bit
+ *   alternates); launches that may run at the same time need separate
+ *   words.  A grid barrier that does not open within about a second sets
+ *   bit 2 of the device fault word (outputs then undefined); zero the word
+ *   again before the next launch.
+ * One cooperative launch, one CTA per SM; every wait in it is bounded.
+ * Requires 1 <= T <= 8 (else MMVQ_ERR_NCOLS), 1 <= k, T*k <= 256,
+ * 1 <= n_experts <= 1024 (else MMVQ_ERR_ROUTING), H and F multiples of 256
+ * in [256, 16384], and a CTA's ring of at least two stages plus the staged
+ * columns of one group (up to 8 x max(H, F) quants) within shared memory,
+ * else MMVQ_ERR_SHAPE (mmvq_expert_ffn_shape tells).  No counterpart on the pages (their engine launches the
+ * steps one by one).
+ */
+MMVQ_API int mmvq_expert_ffn(int type, const void* W_gate_up, const void* W_down, int n_experts,
+                             int H, int F, const float* x, int64_t ldx, int T,
+                             const int32_t* topk, int k, float* gu, void* hq, float* y,
+                             int32_t* expert_ids, int32_t* token_offsets, int32_t* act_index,
+                             int32_t* slot_of, void* xq, int32_t* status, uint32_t* sync,
+                             mmvq_stream_t stream);
+
+/*
+ * The launch shape mmvq_expert_ffn picks (host-only; no kernel runs).
+ * info[8] (HOST memory): grid, threads per CTA, dynamic shared bytes, ring
+ * stages, then G (row groups per item) and P (K-slices) of the gate|up
+ * phase and of the down phase.  Same shape rules as mmvq_expert_ffn.
+ */
+MMVQ_API int mmvq_expert_ffn_shape(int type, int n_experts, int H, int F, int T, int k,
+                                   int32_t* info);
+
+/*
  * RMSNorm folded into the Q8_1 quantiser (the opt-in fused norm named in
  * PR #1774 "How it was checked"; the pages give no formula, so the plain RMS
  * norm with a weight vector).  Per column c of x (fp32 [ncols][ldx], ldx >= K):
@@ -283,9 +338,10 @@ MMVQ_API int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t
 
 /*
  * Device fault word of the bulk-copy kernels.  Every wait of those kernels
- * on a shared-memory barrier is bounded (about one second); a wait that
- * runs out sets a bit here (1: barrier wait timed out) instead of hanging,
- * and the kernel returns with its outputs undefined.  Synchronises
+ * on a shared-memory barrier, and of mmvq_expert_ffn on its grid barriers,
+ * is bounded (about one second); a wait that runs out sets a bit here (1: a
+ * shared-memory barrier wait timed out; 2: a grid barrier timed out) instead
+ * of hanging, and the kernel returns with its outputs undefined.  Synchronises
  * `stream`, stores the word in *fault and clears it.  This HOST-pointer
  * call blocks; it is not part of the hot path.  No counterpart on the
  * pages (their kernels have no such waits).
@@ -301,6 +357,17 @@ MMVQ_API int mmvq_read_device_fault(int* fault, mmvq_stream_t stream);
  * checking the failure path on a live GPU; no counterpart on the pages.
  */
 MMVQ_API int mmvq_selftest_wait_timeout(unsigned int limit_us, mmvq_stream_t stream);
+
+/*
+ * Self-test of the grid barrier's bound in mmvq_expert_ffn: one CTA enters
+ * that barrier, on the counter word *sync, as the first of two blocks whose
+ * second is never launched, with a limit of limit_us microseconds
+ * (1..100000).  The wait runs out and sets bit 2 of the device fault word;
+ * nothing faults.  *sync is left changed (use a word of its own).  No
+ * counterpart on the pages.
+ */
+MMVQ_API int mmvq_selftest_grid_barrier_timeout(uint32_t* sync, unsigned int limit_us,
+                                                mmvq_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -123,6 +123,37 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_repack_planar(14, A, 16, 256, A + 8, None) == mmvq.ERR_ALIGN
     assert L.mmvq_gather_planar_rows(A, 16, 256, A, 0, A, None, None) == mmvq.ERR_SHAPE
     assert L.mmvq_gather_planar_rows(A, 16, 256, A, 4, A + 8, None, None) == mmvq.ERR_ALIGN
+    # expert FFN: type, pointer, shape, token and expert-count rules, checked on the host
+    f = [1012, A, A, 256, 2560, 768, A, 2560, 4, A, 8, A, A, A, None, None, None, None, A,
+         None, A, None]
+
+    def ffn(**kw):
+        a = list(f)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.mmvq_expert_ffn(*a)
+    assert ffn(a0=12) == mmvq.ERR_TYPE                       # GGUF experts: use mmvq_grouped
+    assert ffn(a0=1013) == mmvq.ERR_TYPE
+    assert ffn(a1=None) == mmvq.ERR_NULL
+    assert ffn(a20=None) == mmvq.ERR_NULL                    # sync word
+    assert ffn(a12=None) == mmvq.ERR_NULL                    # hq
+    assert ffn(a4=2560 + 128) == mmvq.ERR_SHAPE              # H % 256
+    assert ffn(a5=0) == mmvq.ERR_SHAPE
+    assert ffn(a7=2048) == mmvq.ERR_SHAPE                    # ldx < H
+    assert ffn(a8=0) == mmvq.ERR_NCOLS and ffn(a8=9) == mmvq.ERR_NCOLS
+    assert ffn(a10=0) == mmvq.ERR_SHAPE and ffn(a10=65) == mmvq.ERR_SHAPE   # T*k > 256
+    assert ffn(a3=0) == mmvq.ERR_ROUTING and ffn(a3=1025) == mmvq.ERR_ROUTING
+    assert ffn(a12=A + 4) == mmvq.ERR_ALIGN                  # hq 16-byte
+    assert ffn(a18=A + 4) == mmvq.ERR_ALIGN                  # xq 16-byte
+    assert ffn(a18=None) == mmvq.ERR_NULL                    # xq is required
+    assert ffn(a2=A + 8) == mmvq.ERR_ALIGN
+    info = (ctypes.c_int32 * 8)()
+    assert L.mmvq_expert_ffn_shape(12, 256, 2560, 768, 4, 8, info) == mmvq.ERR_TYPE
+    assert L.mmvq_expert_ffn_shape(1012, 256, 2560, 768, 9, 8, info) == mmvq.ERR_NCOLS
+    assert L.mmvq_expert_ffn_shape(1012, 256, 2560, 768, 4, 8, None) == mmvq.ERR_NULL
+    assert L.mmvq_selftest_grid_barrier_timeout(None, 1000, None) == mmvq.ERR_NULL
+    assert L.mmvq_selftest_grid_barrier_timeout(A + 2, 1000, None) == mmvq.ERR_ALIGN
+    assert L.mmvq_selftest_grid_barrier_timeout(A, 0, None) == mmvq.ERR_SHAPE
 
 
 def test_product_package_does_not_import_the_oracle():
