@@ -58,28 +58,36 @@ __host__ __device__ inline size_t ffn_smem_bytes(int layout, int S, int H, int F
          (size_t)C * kMaxCols * kTileRows * 4;
 }
 
+// The counter's top bit as a barrier finds it: read once per CTA before the
+// first barrier (no barrier instance can flip it before this CTA arrives),
+// then flipped by the CTA itself after each barrier it passes.
+__device__ __forceinline__ uint32_t grid_barrier_phase(const uint32_t* ctr) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  return v & 0x80000000u;
+}
+
 // Barrier over the consumer threads of every CTA of the grid (see above).
 // The CTA's threads meet first; thread 0's add is a release at GPU scope
-// (cumulative over what the CTA's threads wrote before they met) and its
-// polling load an acquire, so the writes of every CTA before the barrier are
-// visible to every CTA after it.  No full fence: one would also wait for the
-// producer's bulk copies in flight.  Returns false when it gave up after
-// limit_ns.
+// (cumulative over what the CTA's threads wrote before they met), issued
+// without waiting for its result, and its polling load an acquire, so the
+// writes of every CTA before the barrier are visible to every CTA after it.
+// No full fence: one would also wait for the producer's bulk copies in
+// flight.  phase: the top bit before this barrier (grid_barrier_phase), updated
+// here.  Returns false when it gave up after limit_ns.
 __device__ __forceinline__ bool grid_barrier_bounded(uint32_t* ctr, uint32_t nblocks,
                                                      int nthreads, volatile int* ok_s,
-                                                     uint64_t limit_ns) {
+                                                     uint64_t limit_ns, uint32_t& phase) {
   group_sync(1, nthreads);
   if (threadIdx.x == 0) {
     const uint32_t inc = blockIdx.x == 0 ? 0x80000000u - (nblocks - 1u) : 1u;
-    uint32_t old;
-    asm volatile("atom.add.release.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(inc)
-                 : "memory");
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(inc) : "memory");
     int ok = 1;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 0;; ++i) {
       uint32_t v;
       asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-      if ((v ^ old) & 0x80000000u) break;
+      if ((v ^ phase) & 0x80000000u) break;
       if ((i & 15u) == 15u && global_ns() - t0 > limit_ns) {
         ok = 0;
         break;
@@ -88,6 +96,7 @@ __device__ __forceinline__ bool grid_barrier_bounded(uint32_t* ctr, uint32_t nbl
     }
     *ok_s = ok;
   }
+  phase ^= 0x80000000u;
   group_sync(1, nthreads);
   return *ok_s != 0;
 }
@@ -139,8 +148,9 @@ __device__ __forceinline__ void ffn_stream(const GroupedRing& r, uint8_t* ring, 
   }
 }
 
-// Consumers: items [it0, it1) of one phase.  stage(p0, n) fills the chunk
-// buffers with the columns of positions p0 .. p0+n-1.
+// Consumers: items [it0, it1) of one phase.  stage(p0, n, first) fills the
+// chunk buffers with the columns of positions p0 .. p0+n-1; first tells that
+// the item is its group's first (row groups from 0).
 template <int LAYOUT, int CM, typename Stage>
 __device__ __forceinline__ void ffn_consume(const GroupedRing& r, int& slot, uint32_t& par,
                                             int warp, int lane, int nthreads, int G, int P,
@@ -166,7 +176,7 @@ __device__ __forceinline__ void ffn_consume(const GroupedRing& r, int& slot, uin
       const int n = min(CM, pe - p0);
       if (grp != staged_grp || p0 != staged_p0) {
         group_sync(1, nthreads);  // the previous columns are no longer read
-        stage(p0, n);
+        stage(p0, n, rgb == 0);
         group_sync(1, nthreads);
         staged_grp = grp;
         staged_p0 = p0;
@@ -248,6 +258,9 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   grid_dependency_wait();  // x and topk may come from the preceding kernel
+  // the barrier word's top bit, as left by earlier launches (read now, used
+  // at the first barrier)
+  uint32_t phase = grid_barrier_phase(a.sync);
   // each consumer warp's first hidden-state value (at most one 32-block per
   // warp for T <= 8 on a full GPU), loaded now so the load overlaps the lists
   const int gwarp = blockIdx.x * C + warp;  // this warp's index in the grid
@@ -327,22 +340,58 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
     const float v = blk == gwarp ? x_first : a.x[(int64_t)t * a.ldx + kb * kQK8 + lane];
     quantize_lane(v, a.xq + (size_t)blk * kQ81Bytes, lane);
   }
-  if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs) &&
+  if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs, phase) &&
       threadIdx.x == 0)
     atomicOr(&g_fault_word, kFaultGridBarrier);
   // 5. gate|up: a group's columns are its tokens' hidden states
   const uint8_t* xq = a.xq;
-  auto stage_gu = [=](int p0, int n) {
+  auto stage_gu = [=](int p0, int n, bool) {
     stage_q8_1<true>(xq, H, n, [=](int c) { return tok_s[p0 + c]; }, act, da,
                      has_min(LAYOUT) ? sa : nullptr, threadIdx.x, nthreads);
   };
   ffn_consume<LAYOUT, CM>(r, slot, par, warp, lane, nthreads, a.g_gu, a.p_gu, H, nrg_gu, nrgb_gu,
                           i0, i1, active, offs_s, act, da, sa, red, a.gu, 2 * F, stage_gu);
-  if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs) &&
+  if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs, phase) &&
       threadIdx.x == 0)
     atomicOr(&g_fault_word, kFaultGridBarrier);
-  // 6. SiLU(gate)*up -> Q8_1, one block per warp over the whole grid
-  {
+  const uint8_t* hq_in = a.hq;
+  if constexpr (CM <= 2) {
+    // 6-7. one or two tokens: a CTA's down work covers one or two positions,
+    // so it requantises their SiLU(gate)*up itself, straight into its staged
+    // columns (no third barrier); the CTA holding a group's first down item
+    // also writes the group's rows of hq
+    auto stage_dn = [=](int p0, int n, bool first) {
+      const int nblk = n * nbq_f;
+      for (int b0 = warp; b0 < nblk; b0 += 4 * C) {
+        float gv[4], uv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int blk = b0 + j * C;
+          if (blk < nblk) {
+            const int q = blk / nbq_f;
+            const float* row = a.gu + (size_t)(p0 + q) * 2 * F + (blk - q * nbq_f) * kQK8 + lane;
+            gv[j] = __ldcg(row);
+            uv[j] = __ldcg(row + F);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int blk = b0 + j * C;
+          if (blk < nblk) {
+            const int q = blk / nbq_f;
+            const int kb = blk - q * nbq_f;
+            quantize_lane_staged(silu_mul(gv[j], uv[j]), act + (size_t)q * act_row_bytes(F),
+                                 da + q * nbq_f, has_min(LAYOUT) ? sa + q * nbq_f : nullptr, kb,
+                                 first ? a.hq + ((size_t)p0 * nbq_f + blk) * kQ81Bytes : nullptr,
+                                 lane);
+          }
+        }
+      }
+    };
+    ffn_consume<LAYOUT, CM>(r, slot, par, warp, lane, nthreads, a.g_dn, a.p_dn, F, nrg_dn,
+                            nrgb_dn, j0, j1, active, offs_s, act, da, sa, red, a.y, H, stage_dn);
+  } else {
+    // 6. SiLU(gate)*up -> Q8_1, one block per warp over the whole grid
     const int nblk = n_pos * nbq_f;
     for (int blk = gwarp; blk < nblk; blk += nwarps) {
       const int q = blk / nbq_f;
@@ -351,18 +400,17 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
       const float h = silu_mul(__ldcg(row + kb * kQK8 + lane), __ldcg(row + F + kb * kQK8 + lane));
       quantize_lane(h, a.hq + (size_t)blk * kQ81Bytes, lane);
     }
+    if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs, phase) &&
+        threadIdx.x == 0)
+      atomicOr(&g_fault_word, kFaultGridBarrier);
+    // 7. down: a group's columns are its positions' requantised activations
+    auto stage_dn = [=](int p0, int n, bool) {
+      stage_q8_1<true>(hq_in, F, n, [=](int c) { return p0 + c; }, act, da,
+                       has_min(LAYOUT) ? sa : nullptr, threadIdx.x, nthreads);
+    };
+    ffn_consume<LAYOUT, CM>(r, slot, par, warp, lane, nthreads, a.g_dn, a.p_dn, F, nrg_dn,
+                            nrgb_dn, j0, j1, active, offs_s, act, da, sa, red, a.y, H, stage_dn);
   }
-  if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs) &&
-      threadIdx.x == 0)
-    atomicOr(&g_fault_word, kFaultGridBarrier);
-  // 7. down: a group's columns are its positions' requantised activations
-  const uint8_t* hq = a.hq;
-  auto stage_dn = [=](int p0, int n) {
-    stage_q8_1<true>(hq, F, n, [=](int c) { return p0 + c; }, act, da,
-                     has_min(LAYOUT) ? sa : nullptr, threadIdx.x, nthreads);
-  };
-  ffn_consume<LAYOUT, CM>(r, slot, par, warp, lane, nthreads, a.g_dn, a.p_dn, F, nrg_dn, nrgb_dn,
-                          j0, j1, active, offs_s, act, da, sa, red, a.y, H, stage_dn);
 }
 
 // ------------------------------------------------------------ host side ----
@@ -514,7 +562,9 @@ int launch_expert_ffn(int type, const FfnArgs& args, cudaStream_t s, int32_t* in
 // word as the kernel does.  The counter word is left changed.
 __global__ void grid_barrier_selftest_kernel(uint32_t* ctr, uint64_t limit_ns) {
   __shared__ volatile int ok_s;
-  if (!grid_barrier_bounded(ctr, 2u, (int)blockDim.x, &ok_s, limit_ns) && threadIdx.x == 0)
+  uint32_t phase = grid_barrier_phase(ctr);
+  if (!grid_barrier_bounded(ctr, 2u, (int)blockDim.x, &ok_s, limit_ns, phase) &&
+      threadIdx.x == 0)
     atomicOr(&g_fault_word, kFaultGridBarrier);
 }
 

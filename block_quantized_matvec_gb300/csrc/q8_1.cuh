@@ -51,6 +51,25 @@ __device__ __forceinline__ void quantize_lane(float v, uint8_t* out, int lane) {
   if (lane == 0) o32[0] = header;
 }
 
+// The same block written into the shared-memory staging layout of the MMVQ
+// kernels (quants at act_col + act_off(kb), d and s as floats into da[kb],
+// sa[kb]; sa may be NULL) and, when out != NULL, also as the 36-byte block
+// at out: the values a kernel stages from that block.
+__device__ __forceinline__ void quantize_lane_staged(float v, uint8_t* act_col, float* da,
+                                                     float* sa, int kb, uint8_t* out, int lane) {
+  uint32_t word, header;
+  quantize_block_warp(v, word, header);
+  if ((lane & 3) == 0) {
+    *reinterpret_cast<uint32_t*>(act_col + act_off(kb) + 4 * (lane >> 2)) = word;
+    if (out) reinterpret_cast<uint32_t*>(out)[1 + (lane >> 2)] = word;
+  }
+  if (lane == 0) {
+    da[kb] = half_bits_to_float((uint16_t)(header & 0xffffu));
+    if (sa) sa[kb] = half_bits_to_float((uint16_t)(header >> 16));
+    if (out) reinterpret_cast<uint32_t*>(out)[0] = header;
+  }
+}
+
 // h = gate/(1+exp(-gate)) * up in fp32 (expf, IEEE division).
 __device__ __forceinline__ float silu_mul(float g, float u) {
   const float sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));

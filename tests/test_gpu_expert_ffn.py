@@ -200,6 +200,17 @@ def test_groups_longer_than_eight_positions():
     _check_synthetic("q4_k_planar", E, H, F, T, k, salt=7, topk=topk)
 
 
+def test_two_tokens_with_a_group_longer_than_a_pass():
+    # T = 2 requantises SiLU*up inside the down staging; a token that repeats
+    # an expert gives a group of six positions, three passes of two
+    E, H, F, T, k = 3, 256, 256, 2, 3
+    topk = np.zeros((T, k), np.int32)
+    topk[1, 1] = 2
+    assert int(oracle.route_groups(topk, E)[1][1]) == 5            # expert 0: 5 positions
+    _check_synthetic("q4_k_planar", E, H, F, T, k, salt=13, topk=topk)
+    _check_synthetic("q6_k_planar", E, H, F, T, k, salt=14, topk=topk)
+
+
 def test_bad_expert_ids_are_dropped_and_flagged():
     E, H, F, T, k = 8, 256, 256, 4, 2
     W_gu, W_dn, x, topk = _synthetic_case("q4_k_planar", E, H, F, T, k, salt=11)
