@@ -83,8 +83,8 @@ WORKLOAD_DESC = {
 }
 
 
-MMVQ_SOURCES = ["api.cu", "common.cuh", "expert_ffn.cuh", "ffn_args.cuh", "kquant.cuh", "mmvq_dense.cu",
-                "mmvq_tma.cu", "q8_1.cuh", "route.cuh", "rowgroup.cuh"]
+MMVQ_SOURCES = ["api.cu", "common.cuh", "expert_ffn.cu", "ffn_args.cuh", "kquant.cuh", "mmvq_dense.cu",
+                "mmvq_tma.cu", "q8_1.cuh", "ring.cuh", "route.cuh", "rowgroup.cuh"]
 
 
 def kernel_source_hash() -> str:

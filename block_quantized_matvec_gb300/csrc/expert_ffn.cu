@@ -34,12 +34,16 @@
 // Every wait is bounded: a barrier that does not open within about a second
 // sets bit 2 of the device fault word and lets the CTA go on (its outputs
 // are then undefined; the word must be zeroed again before the next launch).
-#pragma once
 #ifndef FFN_WARPS12_MAX_T
 #define FFN_WARPS12_MAX_T 2
 #endif
+#include <algorithm>
+#include <mutex>
+#include <unordered_map>
+
 #include "ffn_args.cuh"
 #include "q8_1.cuh"
+#include "ring.cuh"
 #include "route.cuh"
 
 namespace mmvq {
@@ -420,12 +424,14 @@ struct FfnCfg {
   size_t smem;
 };
 
-// Consumer warps per CTA for T tokens.  Measured on GB300 (256 experts,
-// gate|up 1536 x 2560, down 2560 x 768): one 12-warp CTA per SM is faster for
-// one token (15.7 against 17.6 us per layer), three 4-warp CTAs per SM from
-// four tokens on (33.1 / 52.6 us at T = 4 / 8 against 34.1 / 56.8 us): more
-// producers per SM keep more of the larger step's bytes in flight.
-static int ffn_warps(int T) { return T <= FFN_WARPS12_MAX_T ? 12 : 4; }
+// Consumer warps per CTA for CM positions per pass (T rounded up to a power
+// of two).  Measured on GB300 (256 experts, gate|up 1536 x 2560, down
+// 2560 x 768): one 12-warp CTA per SM is faster for one token (15.7 against
+// 17.6 us per layer), three 4-warp CTAs per SM from four tokens on (33.1 /
+// 52.6 us at T = 4 / 8 against 34.1 / 56.8 us): more producers per SM keep
+// more of the larger step's bytes in flight.
+template <int CM>
+constexpr int ffn_warps() { return CM <= FFN_WARPS12_MAX_T ? 12 : 4; }
 
 // (G, P) of one phase: P | K/256, G*P = C, and each warp's K-slice at least
 // three stages long (or all of K when K/256 < 3): items of a stage or two
@@ -539,8 +545,7 @@ static int launch_ffn_fc(FfnArgs args, cudaStream_t stream, int32_t* info) {
 
 template <int LAYOUT, int CM>
 static int launch_ffn_cm(const FfnArgs& args, cudaStream_t stream, int32_t* info) {
-  if (ffn_warps(args.T) == 12) return launch_ffn_fc<LAYOUT, CM, 12>(args, stream, info);
-  return launch_ffn_fc<LAYOUT, CM, 4>(args, stream, info);
+  return launch_ffn_fc<LAYOUT, CM, ffn_warps<CM>()>(args, stream, info);
 }
 
 template <int LAYOUT>
@@ -572,5 +577,8 @@ int launch_grid_barrier_selftest(uint32_t* ctr, uint32_t limit_us, cudaStream_t 
   grid_barrier_selftest_kernel<<<1, 32, 0, stream>>>(ctr, (uint64_t)limit_us * 1000ull);
   return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
 }
+
+// This translation unit's fault word, for mmvq_read_device_fault.
+int read_clear_ffn_fault_word(unsigned int* v) { return read_clear_fault_word(v); }
 
 }  // namespace mmvq

@@ -30,131 +30,18 @@
 #include <mutex>
 #include <unordered_map>
 
-#include "kquant.cuh"
+#include "ring.cuh"
 
 namespace mmvq {
-
-int device_sms();
-size_t max_smem_optin();
-int ensure_smem(const void* kern, size_t smem);
-
-__device__ unsigned int g_fault_word = 0;
-
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
-constexpr int kFaultMbarTimeout = 1;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Waits for the phase with the given parity to complete; false once
-// `limit_ns` (about 1 s by default) has passed.  The timer is read once every
-// 64 tries; `backoff_ns` > 0 sleeps between tries (the producer, whose waits
-// are not on the critical path).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int backoff_ns = 0,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = 0;
-  for (uint32_t i = 1;; ++i) {
-    if (backoff_ns) __nanosleep(backoff_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      const uint64_t t = global_ns();
-      if (t0 == 0) {
-        t0 = t;
-      } else if (t - t0 > limit_ns) {
-        return false;
-      }
-    }
-  }
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Tile bytes of lane L out of a ring slot: the same offsets as in global
-// memory, so each warp-wide 16-byte load covers 512 consecutive bytes.
-__device__ __forceinline__ void load_q6_tile_smem(const uint8_t* tile, int lane, Q6Half& w) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + 512 * j + 16 * lane);
-    w.ql[4 * j + 0] = v.x;
-    w.ql[4 * j + 1] = v.y;
-    w.ql[4 * j + 2] = v.z;
-    w.ql[4 * j + 3] = v.w;
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + 2048 + 512 * j + 16 * lane);
-    w.qh[4 * j + 0] = v.x;
-    w.qh[4 * j + 1] = v.y;
-    w.qh[4 * j + 2] = v.z;
-    w.qh[4 * j + 3] = v.w;
-  }
-  const uint2 s = *reinterpret_cast<const uint2*>(tile + 3072 + 8 * lane);
-  w.sc[0] = s.x;
-  w.sc[1] = s.y;
-  w.d = *reinterpret_cast<const uint16_t*>(tile + 3328 + 2 * (lane & 15));
-}
-
-// Shared memory: [full S][empty S] mbarriers, a fail flag, the ring
-// (S stages of G*P tiles, 128-byte aligned), the activation quants, d_a as
-// floats, the K-slice partials [C][8][16].
-__host__ __device__ inline size_t tma_ring_offset(int S) { return ((size_t)16 * S + 16 + 127) & ~size_t(127); }
-// Layouts whose blocks carry a min term (d*sc*q - dmin*m): the Q8_1 sums s
-// are staged beside d.
-__host__ __device__ constexpr bool has_min(int layout) {
-  return layout == kQ4Planar || layout == kQ5Planar;
-}
-__host__ __device__ constexpr int tile_bytes(int layout) {
-  return layout == kQ4Planar ? kTileBytesQ4 : layout == kQ5Planar ? kTileBytesQ5 : kTileBytes;
-}
-__host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int ncols, int G, int P) {
-  const int C = G * P;
-  return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + (size_t)ncols * act_row_bytes(K) +
-         (size_t)ncols * (K / kQK8) * 4 * (has_min(layout) ? 2 : 1) +
-         (size_t)C * kMaxCols * kTileRows * 4;
-}
-
-__device__ __forceinline__ void group_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 // Consumers are G groups of P warps (C = G*P); warp C is the producer.  A
 // batch is G of the CTA's row groups (group g takes the g-th); within a
 // batch, stage bb holds, for each group, the P consecutive tiles
 // bb*P .. bb*P+P-1 of its row group, and warp (g, p) takes tile bb*P+p.  The
 // P partial sums of a row group are added in warp order at the batch end.
-template <int LAYOUT, int NCOLS>
+// SUMI: also store every per-32-block integer sum (the parity-debug entry);
+// a separate instance, so the product path carries no per-block test.
+template <int LAYOUT, int NCOLS, bool SUMI>
 __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t* __restrict__ W,
                                                                int64_t rows, int K,
                                                                const uint8_t* __restrict__ xq,
@@ -193,9 +80,11 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   __syncthreads();
   grid_launch_dependents();
 
-  // this CTA's row groups: blockIdx.x, + gridDim.x, ...
-  const int64_t my_rgs = (blockIdx.x < n_rg) ? (n_rg - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int64_t batches = (my_rgs + G - 1) / G;
+  // this CTA's row groups: blockIdx.x, + gridDim.x, ... (row groups < 2^27:
+  // 32-bit divisions, which stay inline)
+  const int64_t my_rgs =
+      (blockIdx.x < n_rg) ? (uint32_t)(n_rg - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t batches = (uint32_t)(my_rgs + G - 1) / (uint32_t)G;
   const int64_t total = batches * spb;
 
   if (warp == C) {  // ------------------------------------------ producer
@@ -231,10 +120,10 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
       }
       // no copy of this CTA may land after it exits: wait (bounded) for the
       // last phase of every slot that was filled
-      const int64_t issued = it;
+      const int64_t issued = it;  // a CTA's stages: < 2^31
       for (int s = 0; s < S && s < issued; ++s) {
-        const int64_t last = issued - 1 - ((issued - 1 - s) % S);
-        mbar_wait(&full[s], (uint32_t)((last / S) & 1));
+        const uint32_t last = (uint32_t)(issued - 1) - ((uint32_t)(issued - 1 - s) % (uint32_t)S);
+        mbar_wait(&full[s], (last / (uint32_t)S) & 1u);
       }
     }
     return;
@@ -264,7 +153,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
     const bool valid = k < my_rgs;
     const int64_t rg = blockIdx.x + k * (int64_t)gridDim.x;
     const int64_t row = rg * kTileRows + i;
-    int32_t* srow = (sumi && valid && row < rows) ? sumi + row * nbq : nullptr;
+    int32_t* srow = (SUMI && sumi && valid && row < rows) ? sumi + row * nbq : nullptr;
     if (srow && !waited) {
       grid_dependency_wait();
       waited = true;
@@ -347,111 +236,6 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
 // (item, chunk, stage) sequence, so their slot and phase counters agree.
 
 constexpr int kMaxGroupsTma = 4096;
-
-__device__ __forceinline__ int block_scan_excl(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += n;
-  }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      const int t = warp_sums[w];
-      warp_sums[w] = run;
-      run += t;
-    }
-    warp_sums[nwarps] = run;
-  }
-  __syncthreads();
-  const int out = warp_sums[warp] + x - v;
-  *total = warp_sums[nwarps];
-  __syncthreads();
-  return out;
-}
-
-struct GroupedRing {
-  const uint8_t* ring;
-  size_t stage_bytes;
-  uint64_t* full;
-  uint64_t* empty;
-  volatile int* fail;
-  int S;
-};
-
-// One (item, chunk) for consumer warp (g, p): row group rg, K-slice p.
-template <int LAYOUT, int NC>
-__device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot, uint32_t& par,
-                                                int g, int p, int P, int lane, int spb,
-                                                const uint8_t* act, int rb, const float* da,
-                                                const float* sa, int nbq, float* red,
-                                                float* ybase, int64_t rg, bool valid,
-                                                int64_t rows) {
-  constexpr int TB = tile_bytes(LAYOUT);
-  const int i = lane & 15;
-  const int h = lane >> 4;
-  float acc[NC];
-#pragma unroll
-  for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
-  const size_t tile_off = (size_t)(g * P + p) * TB;
-  for (int bb = 0; bb < spb; ++bb) {
-    const int s = slot;
-    if (!*r.fail && !mbar_wait(&r.full[s], par)) {
-      *r.fail = 1;
-      atomicOr(&g_fault_word, kFaultMbarTimeout);
-    }
-    if (++slot == r.S) {
-      slot = 0;
-      par ^= 1u;
-    }
-    // a row group past the end reads a stale (in-bounds) tile and stores nothing
-    const uint8_t* tile = r.ring + (size_t)s * r.stage_bytes + tile_off;
-    if (LAYOUT == kQ4Planar) {
-      Q4Half w;
-      load_q4_tile_smem(tile, lane, w);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&r.empty[s]);
-      if (valid) q4_dot<NC>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, nullptr, 0);
-    } else {
-      Q6Half w;
-      load_q6_tile_smem(tile, lane, w);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&r.empty[s]);
-      if (valid) q6_dot<NC>(w, h, bb * P + p, act, rb, da, nbq, acc, nullptr, 0);
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < NC; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
-  const int64_t row = rg * kTileRows + i;
-  if (P == 1) {
-    if (valid && h == 0 && row < rows) {
-#pragma unroll
-      for (int c = 0; c < NC; ++c) ybase[c * rows + row] = acc[c];
-    }
-    return;
-  }
-  float* rg_red = red + (size_t)g * P * kMaxCols * kTileRows;
-  if (h == 0) {
-#pragma unroll
-    for (int c = 0; c < NC; ++c) rg_red[(p * kMaxCols + c) * kTileRows + i] = acc[c];
-  }
-  group_sync(2 + g, 32 * P);
-  if (p == 0 && valid && h == 0 && row < rows) {
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      float sum = 0.0f;
-      for (int q = 0; q < P; ++q) sum += rg_red[(q * kMaxCols + c) * kTileRows + i];
-      ybase[c * rows + row] = sum;
-    }
-  }
-  group_sync(2 + g, 32 * P);
-}
 
 __host__ __device__ inline size_t grouped_smem_bytes(int layout, int S, int K, int CM, int G,
                                                      int P) {
@@ -675,7 +459,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
       return MMVQ_OK;
     }
   }
-  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS>;
+  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false>;
   const int sms = device_sms();
   const size_t limit = max_smem_optin();
   if (sms <= 0 || limit == 0) return MMVQ_ERR_CUDA;
@@ -700,6 +484,9 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
           cudaSuccess)
         return MMVQ_ERR_CUDA;
       if (per_sm < 1) continue;
+      // at most three resident CTAs per SM, as measured (a fourth, where
+      // registers allow it, made the one-column head ~6% slower)
+      per_sm = std::min(per_sm, 3);
       const int64_t ctas = std::min<int64_t>((n_rg + G - 1) / G, (int64_t)sms * per_sm);
       best = {G, 1, 2, (int)ctas, smem};
     }
@@ -747,15 +534,27 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
   return MMVQ_OK;
 }
 
-template <int LAYOUT, int NCOLS>
-static int launch_tma_t(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
+// The instance that also stores the per-block sums runs in the product
+// instance's launch shape, so y comes out with the same bits.
+template <int LAYOUT, int NCOLS, bool SUMI>
+static int launch_tma_s(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
                         int32_t* sumi, uint32_t flags, cudaStream_t stream) {
   TmaCfg cfg;
   const int rc = tma_config<LAYOUT, NCOLS>(rows, K, &cfg);
   if (rc != MMVQ_OK) return rc;
-  return launch_pdl(mmvq_planar_tma_kernel<LAYOUT, NCOLS>, dim3(cfg.grid),
+  if (SUMI &&
+      ensure_smem((const void*)mmvq_planar_tma_kernel<LAYOUT, NCOLS, true>, cfg.smem) != MMVQ_OK)
+    return MMVQ_ERR_CUDA;
+  return launch_pdl(mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI>, dim3(cfg.grid),
                     dim3(32 * (cfg.G * cfg.P + 1)), cfg.smem, stream, W, rows, K, xq, y, sumi,
                     cfg.slots, cfg.G, cfg.P, flags);
+}
+
+template <int LAYOUT, int NCOLS>
+static int launch_tma_t(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
+                        int32_t* sumi, uint32_t flags, cudaStream_t stream) {
+  if (sumi) return launch_tma_s<LAYOUT, NCOLS, true>(W, rows, K, xq, y, sumi, flags, stream);
+  return launch_tma_s<LAYOUT, NCOLS, false>(W, rows, K, xq, y, sumi, flags, stream);
 }
 
 template <int LAYOUT>
@@ -984,19 +783,17 @@ int launch_wait_timeout_selftest(uint32_t limit_us, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
 }
 
-// Reads and clears the device fault word (after synchronising `stream`).
+int read_clear_ffn_fault_word(unsigned int* v);
+
+// Reads and clears the device fault words of the ring kernels and of the
+// expert layer (after synchronising `stream`); returns their OR.
 int read_device_fault(int* fault, cudaStream_t stream) {
-  unsigned int v = 0;
+  unsigned int a = 0, b = 0;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MMVQ_ERR_CUDA;
-  if (cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(v)) != cudaSuccess) return MMVQ_ERR_CUDA;
-  const unsigned int zero = 0;
-  if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero)) != cudaSuccess) return MMVQ_ERR_CUDA;
-  *fault = (int)v;
+  if (read_clear_fault_word(&a) != MMVQ_OK || read_clear_ffn_fault_word(&b) != MMVQ_OK)
+    return MMVQ_ERR_CUDA;
+  *fault = (int)(a | b);
   return MMVQ_OK;
 }
 
 }  // namespace mmvq
-
-// The one-launch expert FFN shares this translation unit's ring routines
-// and device fault word.
-#include "expert_ffn.cuh"

@@ -166,8 +166,10 @@ MMVQ_API int mmvq_gemv_ex(int type, const void* W, int64_t rows, int K, const vo
 /*
  * The per-32-block integer sums the dense product forms, for parity checks:
  * sumi: int32 [ncols][rows][K/32], sumi = sc0*sum16 + sc1*sum16 (Q6_K) or
- * sc*sum32 (Q4_K).  Runs the same kernel as mmvq_gemv (with y also written
- * to `y` when y != NULL).  Same argument rules as mmvq_gemv.
+ * sc*sum32 (Q4_K).  Runs mmvq_gemv's kernel code in the same launch shape,
+ * in an instance that also stores the sums (the product instance carries no
+ * such store); y, when y != NULL, gets the same bits as mmvq_gemv gives.
+ * Same argument rules as mmvq_gemv.
  */
 MMVQ_API int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
                           int32_t* sumi, float* y, mmvq_stream_t stream);
