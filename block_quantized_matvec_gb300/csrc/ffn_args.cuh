@@ -1,4 +1,4 @@
-// Arguments of the one-launch expert FFN (expert_ffn.cuh), shared with the
+// Arguments of the one-launch expert FFN (expert_ffn.cu), shared with the
 // C ABI layer.
 #pragma once
 #include <cuda_runtime.h>
