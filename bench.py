@@ -11,11 +11,13 @@ fp32 columns are quantised to Q8_1 once, then every matrix copy gets its
 MMVQ call (several matrices sharing one activation, like q/k/v or gate/up).
 
 The step's calls are made through the public binding and captured once as a
-CUDA graph (the pages' figures are graph replays too, PR #2746), with
-event-record nodes at the boundaries of each case, so each case's MMVQ time
-comes from the timed region itself.  `value` = weight bytes of all calls /
-device time of the step; `e2e` repeats the step with the fp32 columns copied
-in from pinned host memory and all outputs read back every step.
+CUDA graph (the pages' figures are graph replays too, PR #2746).  `value` =
+weight bytes of all calls / device time of that graph's replays.  Per-case
+times come from a second capture of the same calls with event-record nodes at
+the boundaries of each case, replayed after the timed region (an event node
+ends the programmatic chaining of the launches around it, so it stays out of
+the timed graph).  `e2e` repeats the step with the fp32 columns copied in
+from pinned host memory and all outputs read back every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a row sample
@@ -339,20 +341,30 @@ def run_ours(args, rank, world, local_rank):
         run_case(ci)
     torch.cuda.synchronize()
 
-    # the step as one CUDA graph; event nodes at the case boundaries only, so
-    # consecutive MMVQ launches stay chained by programmatic dependent launch
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 * len(case_list))]
-    for e in evs:
-        e.record()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
+    # the step as one CUDA graph, every launch chained to the previous one by
+    # programmatic dependent launch; a second capture of the same calls with
+    # event nodes at the case boundaries gives the per-case times
+    def capture(evs=None, dependent=False):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+            s = torch.cuda.current_stream()
+            for ci in range(len(case_list)):
+                run_case(ci, s, evs, dependent)
+        torch.cuda.synchronize()
+        return g
+
+    def events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 * len(case_list))]
+        for e in evs:
+            e.record()
+        torch.cuda.synchronize()
+        return evs
+
     cap = torch.cuda.Stream(device=dev)
-    cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
-        s = torch.cuda.current_stream()
-        for ci in range(len(case_list)):
-            run_case(ci, s, evs)
-    torch.cuda.synchronize()
+    graph = capture()
+    evs = events()
+    graph_ev = capture(evs)
 
     stream = torch.cuda.current_stream()
     import torch.distributed as dist
@@ -381,31 +393,24 @@ def run_ours(args, rank, world, local_rank):
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     barrier(world)
 
-    # per-case durations from the event nodes of the last step
-    q_us = np.array([evs[3 * ci].elapsed_time(evs[3 * ci + 1]) * 1e3 for ci in range(len(case_list))])
-    g_us = np.array([evs[3 * ci + 1].elapsed_time(evs[3 * ci + 2]) * 1e3
-                     for ci in range(len(case_list))])
+    def case_times(g, ev, runs=5):
+        """Median over replays of (quantise, MMVQ calls) time per case, in us."""
+        for _ in range(2):
+            g.replay()
+        samples = []
+        for _ in range(runs):
+            g.replay()
+            torch.cuda.synchronize()
+            samples.append([[ev[3 * ci + j].elapsed_time(ev[3 * ci + j + 1]) * 1e3 for j in (0, 1)]
+                            for ci in range(len(case_list))])
+        med = np.median(np.array(samples), axis=0)
+        return med[:, 0], med[:, 1]
 
-    # the same calls as a dependent chain (outside the timed region): median
-    # over a few replays of a second graph
-    evd = [torch.cuda.Event(enable_timing=True) for _ in range(3 * len(case_list))]
-    for e in evd:
-        e.record()
-    torch.cuda.synchronize()
-    graph_dep = torch.cuda.CUDAGraph()
-    cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.graph(graph_dep, stream=cap, capture_error_mode="thread_local"):
-        s = torch.cuda.current_stream()
-        for ci in range(len(case_list)):
-            run_case(ci, s, evd, dependent=True)
-    torch.cuda.synchronize()
-    dep_runs = []
-    for _ in range(5):
-        graph_dep.replay()
-        torch.cuda.synchronize()
-        dep_runs.append([evd[3 * ci + 1].elapsed_time(evd[3 * ci + 2]) * 1e3
-                         for ci in range(len(case_list))])
-    d_us = np.median(np.array(dep_runs), axis=0)
+    # per-case durations from the instrumented capture (outside the timed region)
+    q_us, g_us = case_times(graph_ev, evs)
+    # the same calls as a dependent chain: each waits for its predecessor
+    evd = events()
+    _, d_us = case_times(capture(evd, dependent=True), evd)
 
     peak, peak_kind = load_peak()
     w_step = 0
@@ -448,7 +453,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": len(calls),
                    "weight_copies": [len(m) for m in mats],
                    "l2": "weights rotated over copies > 2x L2 per shape (inputs larger than L2)",
-                   "timing": "CUDA graph replay of the step; event nodes at case boundaries",
+                   "timing": "CUDA graph replay of the step (no event nodes inside); per-case "
+                             "times: median of 5 replays of the same calls captured with event "
+                             "nodes at case boundaries, after the timed region",
+                   "instrumented_step_ms": round(float(np.sum(q_us) + np.sum(g_us)) / 1e3, 4),
                    "chain": "calls after a case's first carry the stable-activation flag, so "
                             "consecutive calls overlap; *_dependent per case: the same calls "
                             "without it (each waits for its predecessor), timed after the step",
@@ -460,7 +468,7 @@ def run_ours(args, rank, world, local_rank):
                                  if args.workload == "q6k_sweep" else None),
                      "algorithmic_bytes_per_launch": round(alg_step / len(calls)),
                      "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": "MMVQ kernel, all launches of the last timed step"},
+                     "kernel": "MMVQ kernel, all launches of one step (instrumented replays)"},
         "e2e": {"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
                 "steps": e2e_steps},
