@@ -41,7 +41,8 @@ def test_f16_encode_matches_numpy_on_edges_and_random():
     ])
     x = np.concatenate([v.astype(np.float32), near, -near, rand]).astype(np.float32)
     got = oracle.f32_to_f16_bits(x)
-    ref = x.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):  # values past the fp16 range map to infinity on purpose
+        ref = x.astype(np.float16).view(np.uint16)
     assert np.array_equal(got, ref)
 
 
