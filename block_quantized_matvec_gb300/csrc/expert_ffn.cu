@@ -18,10 +18,12 @@
 //  - The producer streams the CTA's gate|up items and then, through the same
 //    ring, its down items: the down weights are in flight while the
 //    consumers finish gate|up and wait at the grid barriers.
-//  - Three grid barriers over the consumer threads: after the Q8_1 of the
-//    hidden states, after gate|up (every row of every position written), and
-//    after SiLU*up -> Q8_1, which all consumer warps of the grid also share
-//    out block by block.  The producer does not wait at them.
+//  - Grid barriers over the consumer threads: after the Q8_1 of the hidden
+//    states, and after gate|up (every row of every position written).  One
+//    or two tokens: a CTA then requantises the SiLU*up of its down columns
+//    itself while staging them.  Three or more: all consumer warps of the
+//    grid share SiLU*up -> Q8_1 out block by block, behind a third barrier.
+//    The producer does not wait at them.
 // Items, shares and the consume routine are those of the grouped kernel: an
 // item is G row groups of one non-empty group's expert, each CTA takes an
 // equal contiguous range of items per phase, warp (g, p) takes row group g

@@ -264,7 +264,8 @@ MMVQ_API int mmvq_silu_mul_quantize_q8_1(const float* gu, int F, int n, void* xq
  *   words.  A grid barrier that does not open within about a second sets
  *   bit 2 of the device fault word (outputs then undefined); zero the word
  *   again before the next launch.
- * One cooperative launch, one CTA per SM; every wait in it is bounded.
+ * One cooperative launch (one CTA per SM for T <= 2, three from T = 3 on);
+ * every wait in it is bounded.
  * Requires 1 <= T <= 8 (else MMVQ_ERR_NCOLS), 1 <= k, T*k <= 256,
  * 1 <= n_experts <= 1024 (else MMVQ_ERR_ROUTING), H and F multiples of 256
  * in [256, 16384], and a CTA's ring of at least two stages plus the staged
