@@ -442,10 +442,15 @@ struct TmaCfg {
 
 // Launch shape.  Candidates (G, P) with P | K/256 and C = G*P <= 12; the ring
 // gets as many stages as fit in ~110 KB (two CTAs per SM when registers
-// allow), at least two.  Cost model: a CTA's time is its batches x stages
-// per batch, each stage one tile per consumer warp; the SM's issue rate is
-// shared by all resident consumer warps.  The cheapest shape wins; ties go
-// to more consumer warps.
+// allow), at least two.  Cost model: a CTA's time is its batches x (stages
+// per batch + the batch's K-slice reduction over P warps, (P-1)/18 of a
+// stage), each stage one tile per consumer warp; the SM's issue rate is
+// shared by all resident consumer warps once they exceed 20.  The cheapest
+// shape wins; ties go to more consumer warps.  The two constants were fitted
+// on GB300 to every (G, P) of the Q6_K 2560 x 2560, 2560 x 10240 and
+// 10240 x 2560 calls at 1-8 columns, timed back to back and as a dependent
+// chain: they pick G = 2, P = 5 over G = 1, P = 10 for 10240 x 2560 at 1-4
+// columns (one batch per CTA instead of three), faster in both timings.
 template <int LAYOUT, int NCOLS>
 static int tma_config(int64_t rows, int K, TmaCfg* out) {
   static std::mutex mu;
@@ -517,9 +522,9 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
       const int64_t batches = (rgs_per_cta + G - 1) / G;
       const double ctas_per_sm = std::min<double>(per_sm, (double)ctas / sms);
       const double warps_per_sm = std::max(1.0, ctas_per_sm) * G * P;
-      // stage time: one tile per warp, slowed once the SM holds > 16 warps
-      const double stage = std::max(1.0, warps_per_sm / 16.0);
-      const double cost = (double)batches * (nb / P) * stage;
+      // stage time: one tile per warp, slowed once the SM holds > 20 warps
+      const double stage = std::max(1.0, warps_per_sm / 20.0);
+      const double cost = (double)batches * ((double)(nb / P) + (P - 1) / 18.0) * stage;
       if (cost < best_cost * 0.999 || (cost < best_cost * 1.001 && G * P > best_c)) {
         best_cost = cost;
         best_c = G * P;
