@@ -432,7 +432,10 @@ def run_ours(args, rank, world, local_rank):
                          "weight_gbps_dependent": round(wb / du / 1e3, 1)})
     step_s = elapsed_ms / 1e3 / args.steps
     value = world * w_step / step_s / 1e9
-    achieved = alg_step / (float(np.sum(g_us)) * 1e-6) / 1e9
+    # the MMVQ launches' algorithmic bytes over the timed step (which also
+    # holds one Q8_1 launch per case: a conservative figure)
+    achieved = alg_step / step_s / 1e9
+    achieved_instr = alg_step / (float(np.sum(g_us)) * 1e-6) / 1e9
 
     # e2e: H2D of the step's columns, the step, D2H of every output, each step
     e2e_steps = max(3, min(args.steps, 200))
@@ -468,7 +471,9 @@ def run_ours(args, rank, world, local_rank):
                                  if args.workload == "q6k_sweep" else None),
                      "algorithmic_bytes_per_launch": round(alg_step / len(calls)),
                      "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": "MMVQ kernel, all launches of one step (instrumented replays)"},
+                     "kernel": "MMVQ kernel, all launches of the timed step (its one Q8_1 launch "
+                               "per case counted in the time)",
+                     "achieved_instrumented": round(achieved_instr, 1)},
         "e2e": {"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
                 "steps": e2e_steps},
