@@ -42,8 +42,8 @@ def test_swar_offset_equals_per_byte_subtraction_on_every_packed_word():
 
 
 def test_the_check_catches_a_wrong_constant():
-    # a subtrahend off by one in one byte, or a mask that misses the guard
-    # bit, breaks the identity somewhere in the 64^4 words
+    # a subtrahend off by one in one byte, a mask that misses the guard bit,
+    # or no final flip: each breaks the identity on some of these words
     a, b, c = _kernel_constants()
     codes = np.arange(64, dtype=np.uint32)
     w = (codes[:, None] | (codes[None, :] << 8)).reshape(-1) | np.uint32(0x1f1f0000)
