@@ -10,7 +10,6 @@
 // crosses into the next group.  Each item runs the dense row-group routine
 // with as many columns as the group has positions (up to 8 at a time).
 #include <algorithm>
-#include <mutex>
 
 #include "rowgroup.cuh"
 
@@ -184,7 +183,6 @@ static int launch_grouped_t(const uint8_t* W, int n_experts, int64_t rows, int K
     smem = mmvq_smem_bytes(LAYOUT, K, kMaxCols, wk);
   }
   if (smem > limit) return MMVQ_ERR_SHAPE;
-  static std::mutex mu;
   if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * wk, smem) != cudaSuccess ||
