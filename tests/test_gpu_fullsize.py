@@ -87,3 +87,24 @@ def test_lm_head_and_draft_head():
         _check_sampled(mmvq.TYPE_Q6_K_PLANAR, oracle.TYPE_Q6_K, W, P, rows, K, x, ncols, ncols)
         _check_sampled(mmvq.TYPE_Q6_K_PLANAR, oracle.TYPE_Q6_K, Wdraft, D, 4096, K, x, ncols,
                        ncols)
+
+
+@pytest.mark.parametrize("kind,rows,K", [("q6_k", 10247, 2560), ("q4_k", 12300, 2560),
+                                         ("q5_k", 6151, 2560)])
+def test_tall_ragged_matrices_with_several_row_groups_per_cta(kind, rows, K):
+    # row counts just past a 16-row multiple, at sizes where the launch shape
+    # gives each CTA more than one row group (G > 1); the sample holds the
+    # last, partial row group
+    gen = {"q6_k": synth.q6_k_weights, "q4_k": synth.q4_k_weights, "q5_k": synth.q5_k_weights}[kind]
+    src = {"q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K, "q5_k": mmvq.TYPE_Q5_K}[kind]
+    t = {"q6_k": mmvq.TYPE_Q6_K_PLANAR, "q4_k": mmvq.TYPE_Q4_K_PLANAR,
+         "q5_k": mmvq.TYPE_Q5_K_PLANAR}[kind]
+    t_orc = {"q6_k": oracle.TYPE_Q6_K, "q4_k": oracle.TYPE_Q4_K, "q5_k": oracle.TYPE_Q5_K}[kind]
+    W = gen(rows, K, salt=rows)
+    Wd = mmvq.repack_planar(dev(W), rows, K, type_=src)
+    groups = []
+    for ncols in (1, 2, 4):
+        groups.append(mmvq.launch_shape(t, rows, K, ncols)["G"])
+        x = synth.activations(K, ncols, salt=30 + ncols)
+        _check_sampled(t, t_orc, W, Wd, rows, K, x, ncols, salt=ncols)
+    assert max(groups) > 1, groups
