@@ -182,7 +182,8 @@ MMVQ_API int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K,
  * with each expert repacked on its own and rows a multiple of 16).  Group g (0 <= g < n_groups) multiplies
  * expert expert_ids[g] with the activation columns of positions
  * p in [token_offsets[g], token_offsets[g+1]); column act_index[p] of xq
- * (column p when act_index == NULL).  Output row p: y[p][0..rows).
+ * (column p when act_index == NULL).  Output row p: y[p][0..rows); rows of
+ * positions outside every group are not written.
  * xq: [n_xq_cols][K/32] Q8_1 blocks.  Empty groups are legal and cost
  * nothing.  Groups may hold any number of positions (processed 8 at a time).
  * Device-side checks: an expert id outside [0, n_experts), decreasing
