@@ -1,12 +1,13 @@
-// Planar (Q6_K and Q4_K tile) MMVQ fed by bulk copies (cp.async.bulk, the 1-D TMA path) into
-// a shared-memory ring ("Strata" PR #2340 "STRATA_Q6_PLANAR": the head's
+// Planar (Q6_K, Q4_K and Q5_K tile) MMVQ fed by bulk copies (cp.async.bulk, the 1-D TMA path)
+// into a shared-memory ring ("Strata" PR #2340 "STRATA_Q6_PLANAR": the head's
 // planes are laid out so every lane load is one aligned 16-byte load; PR
 // #2207: the weights are read once for all 1-8 columns).
 //
 // GB300 design.  One producer warp per CTA streams the CTA's weights from
-// HBM into a ring of S stages with one bulk copy per stage; a stage is C
-// consecutive 3360-byte tiles (16 rows x one 256-block each) of one row
-// group, one tile per consumer warp.  Each stage has a pair of mbarriers
+// HBM into a ring of S stages; a stage holds, for each of the batch's G row
+// groups, P consecutive tiles (16 rows x one 256-block each: 3360 bytes for
+// Q6_K, 2304 for Q4_K, 2816 for Q5_K), one bulk copy per row group, one tile
+// per consumer warp.  Each stage has a pair of mbarriers
 // (full: bytes landed; empty: all C consumer warps have read it).  The bytes
 // in flight per SM are set by the ring depth, not by how many warps hold
 // loads in registers.  Every consumer warp walks every stage in order, so a
