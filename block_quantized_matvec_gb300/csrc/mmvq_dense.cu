@@ -163,7 +163,12 @@ struct DenseCfg {
 //  - many row groups (>= 8 per SM): one warp per row group, 8 per CTA,
 //    persistent grid of (CTAs resident per SM) x SMs;
 //  - otherwise the largest K-split WK (a divisor of K/256, at most 16 warps)
-//    that still keeps every row group's CTA resident in a single wave.
+//    that still keeps every row group's CTA resident in a single wave;
+//  - unless that leaves each warp more than 8 blocks of K (wide activations
+//    crowd the shared memory out, so only small WK fit in one wave): then
+//    the WK with the fewest waves x K/256/WK, ties to fewer waves.  Measured
+//    on GB300: 2560 x 10240 at 8 columns took 110.6 us at WK = 1 (one wave)
+//    and 41.7 us at WK = 10 (two waves).
 template <int LAYOUT, int NCOLS>
 static int dense_config(int64_t rows, int K, DenseCfg* out) {
   static std::mutex mu;
@@ -205,6 +210,25 @@ static int dense_config(int64_t rows, int K, DenseCfg* out) {
       if (n_rg <= (int64_t)sms * per_sm) {
         cfg = {wk, 1, (int)n_rg, smem};
         break;
+      }
+    }
+  }
+  if (cfg.wk != 0 && nb / cfg.wk > 8) {
+    int64_t best = nb / cfg.wk;  // one wave
+    int64_t best_waves = 1;
+    for (int wk = std::min(nb, 16); wk > cfg.wk; --wk) {
+      if (nb % wk) continue;
+      const size_t smem = mmvq_smem_bytes(LAYOUT, K, NCOLS, wk);
+      int per_sm = 0;
+      const int rc = occupancy(wk, smem, &per_sm);
+      if (rc == MMVQ_ERR_CUDA) return rc;
+      if (rc != MMVQ_OK || per_sm < 1) continue;
+      const int64_t waves = (n_rg + (int64_t)sms * per_sm - 1) / ((int64_t)sms * per_sm);
+      const int64_t cost = waves * (nb / wk);
+      if (cost < best || (cost == best && waves < best_waves)) {
+        best = cost;
+        best_waves = waves;
+        cfg = {wk, 1, (int)n_rg, smem};
       }
     }
   }
