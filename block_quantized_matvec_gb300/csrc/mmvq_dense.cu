@@ -19,6 +19,7 @@
 // mid-size matrices are resident in one wave; large ones run persistently
 // and prefetch the next row group into L2 while computing the current one.
 #include <algorithm>
+#include <cstdint>
 #include <map>
 #include <mutex>
 #include <unordered_map>
@@ -164,11 +165,13 @@ struct DenseCfg {
 //    persistent grid of (CTAs resident per SM) x SMs;
 //  - otherwise the largest K-split WK (a divisor of K/256, at most 16 warps)
 //    that still keeps every row group's CTA resident in a single wave;
-//  - unless that leaves each warp more than 8 blocks of K (wide activations
-//    crowd the shared memory out, so only small WK fit in one wave): then
-//    the WK with the fewest waves x K/256/WK, ties to fewer waves.  Measured
-//    on GB300: 2560 x 10240 at 8 columns took 110.6 us at WK = 1 (one wave)
-//    and 41.7 us at WK = 10 (two waves).
+//  - unless no WK fits in one wave, or the one that does leaves each warp
+//    more than 8 blocks of K (wide activations crowd the shared memory out):
+//    then the WK with the fewest waves x K/256/WK, ties to fewer waves.
+//    Measured on GB300: 2560 x 10240 at 8 columns took 110.6 us at WK = 1
+//    (one wave) and 41.7 us at WK = 10 (two waves); 2560 x 16384 at 8
+//    columns 192.8 us on the persistent shape (20 CTAs) and 66.2 us at
+//    WK = 8 (two waves).
 template <int LAYOUT, int NCOLS>
 static int dense_config(int64_t rows, int K, DenseCfg* out) {
   static std::mutex mu;
@@ -213,9 +216,10 @@ static int dense_config(int64_t rows, int K, DenseCfg* out) {
       }
     }
   }
-  if (cfg.wk != 0 && nb / cfg.wk > 8) {
-    int64_t best = nb / cfg.wk;  // one wave
-    int64_t best_waves = 1;
+  if (n_rg < (int64_t)sms * 8 && (cfg.wk == 0 || nb / cfg.wk > 8)) {
+    // the one-wave choice, if any, against every larger K-split
+    int64_t best = cfg.wk != 0 ? nb / cfg.wk : INT64_MAX;
+    int64_t best_waves = cfg.wk != 0 ? 1 : INT64_MAX;
     for (int wk = std::min(nb, 16); wk > cfg.wk; --wk) {
       if (nb % wk) continue;
       const size_t smem = mmvq_smem_bytes(LAYOUT, K, NCOLS, wk);
