@@ -548,6 +548,8 @@ static int launch_tma_s(const uint8_t* W, int64_t rows, int K, const uint8_t* xq
   TmaCfg cfg;
   const int rc = tma_config<LAYOUT, NCOLS>(rows, K, &cfg);
   if (rc != MMVQ_OK) return rc;
+  // the ring needs at least two stages (the chooser never picks fewer)
+  if (cfg.slots < 2 || cfg.G < 1 || cfg.P < 1 || cfg.G * cfg.P > 12) return MMVQ_ERR_SHAPE;
   if (SUMI &&
       ensure_smem((const void*)mmvq_planar_tma_kernel<LAYOUT, NCOLS, true>, cfg.smem) != MMVQ_OK)
     return MMVQ_ERR_CUDA;
