@@ -58,6 +58,9 @@ const char* mmvq_strerror(int code) {
     case MMVQ_ERR_ALIGN: return "a pointer breaks its alignment rule (16 B for W/xq/out, 4 B otherwise)";
     case MMVQ_ERR_ROUTING: return "routing lists rejected";
     case MMVQ_ERR_CUDA: return "CUDA launch failed (no usable sm_103a device?)";
+    case MMVQ_ERR_SCRATCH:
+      return "the layer's intermediates exceed the fixed scratch of mmvq_expert_ffn_noalloc "
+             "(MMVQ_NOALLOC_SCRATCH_BYTES)";
   }
   return "unknown mmvq status";
 }
@@ -211,6 +214,41 @@ int mmvq_expert_ffn(int type, const void* W_gate_up, const void* W_down, int n_e
   a.status = status;
   a.sync = sync;
   return mmvq::launch_expert_ffn(type, a, (cudaStream_t)stream, nullptr);
+}
+
+int mmvq_expert_ffn_noalloc(int type, const void* W_gate_up, const void* W_down, int n_experts,
+                            int H, int F, const float* x, int64_t ldx, int T,
+                            const int32_t* topk, int k, float* y, int32_t* expert_ids,
+                            int32_t* token_offsets, int32_t* act_index, int32_t* slot_of,
+                            int32_t* status, mmvq_stream_t stream) {
+  int rc = check_expert_ffn(type, W_gate_up, W_down, n_experts, H, F, x, ldx, T, topk, k);
+  if (rc) return rc;
+  if (!y) return MMVQ_ERR_NULL;
+  if (!aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(x, 4) || !aligned(topk, 4) ||
+      !aligned(y, 4) || (expert_ids && !aligned(expert_ids, 4)) ||
+      (token_offsets && !aligned(token_offsets, 4)) || (act_index && !aligned(act_index, 4)) ||
+      (slot_of && !aligned(slot_of, 4)) || (status && !aligned(status, 4)))
+    return MMVQ_ERR_ALIGN;
+  static_assert(mmvq::kFfnScratchBytes == MMVQ_NOALLOC_SCRATCH_BYTES, "scratch size");
+  if (mmvq::ffn_scratch_layout(H, F, T, k).end > mmvq::kFfnScratchBytes) return MMVQ_ERR_SCRATCH;
+  mmvq::FfnArgs a = {};
+  a.w_gu = static_cast<const uint8_t*>(W_gate_up);
+  a.w_dn = static_cast<const uint8_t*>(W_down);
+  a.n_experts = n_experts;
+  a.H = H;
+  a.F = F;
+  a.x = x;
+  a.ldx = ldx;
+  a.T = T;
+  a.topk = topk;
+  a.k = k;
+  a.y = y;
+  a.expert_ids = expert_ids;
+  a.offsets = token_offsets;
+  a.act_index = act_index;
+  a.slot_of = slot_of;
+  a.status = status;
+  return mmvq::launch_expert_ffn_noalloc(type, a, (cudaStream_t)stream);
 }
 
 int mmvq_expert_ffn_shape(int type, int n_experts, int H, int F, int T, int k, int32_t* info) {

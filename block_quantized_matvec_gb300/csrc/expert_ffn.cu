@@ -580,6 +580,53 @@ int launch_grid_barrier_selftest(uint32_t* ctr, uint32_t limit_us, cudaStream_t 
   return cudaGetLastError() == cudaSuccess ? MMVQ_OK : MMVQ_ERR_CUDA;
 }
 
+// ----------------------------------------------- fixed-scratch variant ----
+//
+// mmvq_expert_ffn_noalloc keeps the layer's intermediates (the barrier word,
+// xq, hq and gu) in this array instead of buffers from the caller.  It is a
+// file-scope device variable, so every GPU that loads the library holds it
+// until the process exits, and every call on a device shares it.  Host code
+// must not hand the name itself to a kernel (on the host it names a
+// stand-in, not device memory): its device address is looked up once per
+// device with cudaGetSymbolAddress, with that device current, and cached.
+static __device__ __align__(256) uint8_t g_ffn_scratch[kFfnScratchBytes];
+
+static int ffn_scratch_address(uint8_t** p) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return MMVQ_ERR_CUDA;
+  static std::mutex mu;
+  static std::unordered_map<int, uint8_t*> addr;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = addr.find(dev);
+  if (it != addr.end()) {
+    *p = it->second;
+    return MMVQ_OK;
+  }
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_ffn_scratch) != cudaSuccess || ptr == nullptr)
+    return MMVQ_ERR_CUDA;
+  addr[dev] = static_cast<uint8_t*>(ptr);
+  *p = static_cast<uint8_t*>(ptr);
+  return MMVQ_OK;
+}
+
+int launch_expert_ffn_noalloc(int type, FfnArgs a, cudaStream_t s) {
+  const FfnScratchLayout l = ffn_scratch_layout(a.H, a.F, a.T, a.k);
+  if (l.end > kFfnScratchBytes) return MMVQ_ERR_SCRATCH;
+  uint8_t* base = nullptr;
+  const int rc = ffn_scratch_address(&base);
+  if (rc != MMVQ_OK) return rc;
+  a.sync = reinterpret_cast<uint32_t*>(base);
+  a.xq = base + l.xq;
+  a.hq = base + l.hq;
+  a.gu = reinterpret_cast<float*>(base + l.gu);
+  // the grid barrier needs a word whose low 31 bits are zero; a launch that
+  // gave up at a barrier leaves it otherwise, so it is cleared every call
+  // (xq, hq and gu are written before they are read)
+  if (cudaMemsetAsync(a.sync, 0, sizeof(uint32_t), s) != cudaSuccess) return MMVQ_ERR_CUDA;
+  return launch_expert_ffn(type, a, s, nullptr);
+}
+
 // This translation unit's fault word, for mmvq_read_device_fault.
 int read_clear_ffn_fault_word(unsigned int* v) { return read_clear_fault_word(v); }
 

@@ -33,4 +33,28 @@ struct FfnArgs {
 int launch_expert_ffn(int type, const FfnArgs& args, cudaStream_t s, int32_t* info);
 int launch_grid_barrier_selftest(uint32_t* ctr, uint32_t limit_us, cudaStream_t stream);
 
+// mmvq_expert_ffn_noalloc: the layer's intermediates live in one fixed
+// device array of kFfnScratchBytes (expert_ffn.cu), carved as
+// [barrier word | xq | hq | gu], each part starting on a 256-byte boundary.
+constexpr size_t kFfnScratchBytes = (size_t)2 << 20;
+
+struct FfnScratchLayout {
+  size_t xq, hq, gu, end;  // byte offsets; the barrier word sits at 0
+};
+
+inline FfnScratchLayout ffn_scratch_layout(int H, int F, int T, int k) {
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  const size_t n = (size_t)T * (size_t)k;
+  FfnScratchLayout l;
+  l.xq = 256;
+  l.hq = l.xq + up((size_t)T * (size_t)(H / 32) * 36);
+  l.gu = l.hq + up(n * (size_t)(F / 32) * 36);
+  l.end = l.gu + n * 2 * (size_t)F * sizeof(float);
+  return l;
+}
+
+// Fills args.sync, xq, hq and gu from the fixed array of the current device
+// and launches as launch_expert_ffn does.
+int launch_expert_ffn_noalloc(int type, FfnArgs args, cudaStream_t s);
+
 }  // namespace mmvq

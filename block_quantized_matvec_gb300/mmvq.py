@@ -30,6 +30,8 @@ MAX_COLS = 8
 OK = 0
 FLAG_XQ_STABLE = 1
 ERR_TYPE, ERR_SHAPE, ERR_NCOLS, ERR_NULL, ERR_ALIGN, ERR_ROUTING, ERR_CUDA = -1, -2, -3, -4, -5, -6, -7
+ERR_SCRATCH = -8
+NOALLOC_SCRATCH_BYTES = 2 << 20  # MMVQ_NOALLOC_SCRATCH_BYTES
 
 # name -> (restype, argtypes); mirrors include/mmvq.h
 _P, _I, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
@@ -53,6 +55,8 @@ SIGNATURES = {
     "mmvq_launch_shape": (_I, [_I, _I64, _I, _I, _P]),
     "mmvq_expert_ffn": (_I, [_I, _P, _P, _I, _I, _I, _P, _I64, _I, _P, _I, _P, _P, _P, _P, _P,
                              _P, _P, _P, _P, _P, _P]),
+    "mmvq_expert_ffn_noalloc": (_I, [_I, _P, _P, _I, _I, _I, _P, _I64, _I, _P, _I, _P, _P, _P,
+                                     _P, _P, _P, _P]),
     "mmvq_expert_ffn_shape": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "mmvq_selftest_grid_barrier_timeout": (_I, [_P, ctypes.c_uint, _P]),
 }
@@ -247,6 +251,40 @@ def expert_ffn(type_: int, W_gate_up: torch.Tensor, W_down: torch.Tensor, n_expe
                                  _ptr(out.get("act_index")), _ptr(out.get("slot_of")),
                                  _ptr(xq), _ptr(status), _ptr(sync), _stream(stream)),
            "mmvq_expert_ffn")
+    return out
+
+
+def expert_ffn_noalloc(type_: int, W_gate_up: torch.Tensor, W_down: torch.Tensor,
+                       n_experts: int, H: int, F: int, x: torch.Tensor, topk: torch.Tensor, *,
+                       y: torch.Tensor | None = None, lists: bool = True,
+                       status: torch.Tensor | None = None, stream=None) -> dict:
+    """expert_ffn with its intermediates (xq, gu, hq, barrier word) in the library's
+    fixed device array: for callers that cannot allocate.  Pass y (and the list
+    outputs) preallocated to allocate nothing here either.  Returns y and, with
+    lists=True, expert_ids, offsets, act_index, slot_of."""
+    for t, n in ((W_gate_up, "W_gate_up"), (W_down, "W_down"), (x, "x"), (topk, "topk")):
+        _dev(t, n)
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    T, k = topk.shape
+    n = T * k
+    dev = x.device
+    if y is None:
+        y = torch.empty((n, H), dtype=torch.float32, device=dev)
+    out = {"y": y}
+    if lists:
+        out.update(expert_ids=torch.empty(n_experts, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(n_experts + 1, dtype=torch.int32, device=dev),
+                   act_index=torch.empty(max(n, 1), dtype=torch.int32, device=dev),
+                   slot_of=torch.empty(max(n, 1), dtype=torch.int32, device=dev))
+    if status is not None:
+        out["status"] = status
+    _check(lib().mmvq_expert_ffn_noalloc(type_, _ptr(W_gate_up), _ptr(W_down), n_experts, H, F,
+                                         _ptr(x), x.stride(0), T, _ptr(topk), k, _ptr(y),
+                                         _ptr(out.get("expert_ids")), _ptr(out.get("offsets")),
+                                         _ptr(out.get("act_index")), _ptr(out.get("slot_of")),
+                                         _ptr(status), _stream(stream)),
+           "mmvq_expert_ffn_noalloc")
     return out
 
 

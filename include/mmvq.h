@@ -6,7 +6,8 @@
  *  - Pointers named W (W_*), xq, hq, x, y, gu, sumi, row_ids, topk,
  *    expert_ids, token_offsets, act_index, slot_of, status, sync and out are
  *    DEVICE pointers, owned by the caller, who allocates and frees them.  The library allocates no
- *    device or host memory and never synchronises the stream.
+ *    device or host memory and never synchronises the stream (its one
+ *    device buffer is the fixed array of mmvq_expert_ffn_noalloc).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream).  Launch failures are reported by the return
  *    value; faults inside a kernel surface at the caller's next sync.
@@ -118,7 +119,8 @@ enum mmvq_status {
   MMVQ_ERR_NULL = -4,    /* a required pointer is NULL */
   MMVQ_ERR_ALIGN = -5,   /* a pointer breaks its alignment rule */
   MMVQ_ERR_ROUTING = -6, /* routing lists rejected (host-side limits) */
-  MMVQ_ERR_CUDA = -7     /* a CUDA launch or attribute call failed */
+  MMVQ_ERR_CUDA = -7,    /* a CUDA launch or attribute call failed */
+  MMVQ_ERR_SCRATCH = -8  /* mmvq_expert_ffn_noalloc: intermediates exceed its fixed scratch */
 };
 
 /* Version of this ABI (major*10000 + minor*100 + patch). */
@@ -280,6 +282,45 @@ MMVQ_API int mmvq_expert_ffn(int type, const void* W_gate_up, const void* W_down
                              int32_t* expert_ids, int32_t* token_offsets, int32_t* act_index,
                              int32_t* slot_of, void* xq, int32_t* status, uint32_t* sync,
                              mmvq_stream_t stream);
+
+/*
+ * mmvq_expert_ffn for callers that cannot allocate device memory.  Some
+ * callers only ever hold the buffers of their own tensors: a plugin inside
+ * an inference engine whose memory pool owns the whole device, or a C
+ * caller that was handed device pointers and has no allocator of its own.
+ * Others must keep cudaMalloc, which can synchronise the device, out of a
+ * decode step.  For them the layer's intermediates (the grid-barrier word,
+ * the Q8_1 hidden states xq, the gate|up rows gu and the requantised hq)
+ * live in one fixed device array of MMVQ_NOALLOC_SCRATCH_BYTES inside the
+ * library; the caller passes only inputs and outputs.  The pages have no
+ * counterpart (their engine allocates its buffers).
+ *   Arguments, limits and results are those of mmvq_expert_ffn, without
+ *   gu, hq, xq and sync.  y gets the same bits as mmvq_expert_ffn gives for
+ *   the same inputs.
+ *   Size limit: the parts, each rounded up to 256 bytes, must fit:
+ *   256 + T*(H/32)*36 + T*k*(F/32)*36 + T*k*2F*4 <= MMVQ_NOALLOC_SCRATCH_BYTES
+ *   (2 MiB; the pages' layer, H = 2560, F = 768, T = 8, k = 8, takes
+ *   about 0.5 MiB), else MMVQ_ERR_SCRATCH before any CUDA call.
+ *   Memory: every GPU that loads the library holds the array until the
+ *   process exits.  The call allocates nothing and frees nothing; it clears
+ *   the barrier word with cudaMemsetAsync on `stream` before the launch.
+ *   Set-up: the first call on a device, with that device current, looks up
+ *   the array's device address (cudaGetSymbolAddress) and caches it; make
+ *   that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, which keeps the
+ *   last call's intermediates.  Calls that may run at the same time on one
+ *   device (other streams, other host threads) race on it and give
+ *   undefined results; calls in order on one stream are safe.
+ */
+MMVQ_API int mmvq_expert_ffn_noalloc(int type, const void* W_gate_up, const void* W_down,
+                                     int n_experts, int H, int F, const float* x, int64_t ldx,
+                                     int T, const int32_t* topk, int k, float* y,
+                                     int32_t* expert_ids, int32_t* token_offsets,
+                                     int32_t* act_index, int32_t* slot_of, int32_t* status,
+                                     mmvq_stream_t stream);
+
+/* Size of the fixed scratch array of mmvq_expert_ffn_noalloc, per device. */
+#define MMVQ_NOALLOC_SCRATCH_BYTES (2u << 20)
 
 /*
  * The launch shape mmvq_expert_ffn picks (host-only; no kernel runs).

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_strerror(lib):
     assert lib.mmvq_version() == 10000
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert mmvq.strerror(code) and "unknown" not in mmvq.strerror(code)
     assert "unknown" in mmvq.strerror(-99)
 
