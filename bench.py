@@ -19,6 +19,11 @@ ends the programmatic chaining of the launches around it, so it stays out of
 the timed graph).  `e2e` repeats the step with the fp32 columns copied in
 from pinned host memory and all outputs read back every step.
 
+The default run also times the pages' other matrices (the LM head and the
+gathered draft head at 1-5 columns, the Q4_K and Q5_K dense shapes, the MoE
+layer at T = 1, 4, 8), each as its own workload with fewer steps, and adds
+their summaries under `workloads` (`--no-extra` leaves them out).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a row sample
 
@@ -438,7 +443,8 @@ def run_ours(args, rank, world, local_rank):
     achieved_instr = alg_step / (float(np.sum(g_us)) * 1e-6) / 1e9
 
     # e2e: H2D of the step's columns, the step, D2H of every output, each step
-    e2e_steps = max(3, min(args.steps, 200))
+    # (left out for the extra workloads of the default run)
+    e2e_steps = 0 if getattr(args, "light", False) else max(3, min(args.steps, 200))
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -446,7 +452,7 @@ def run_ours(args, rank, world, local_rank):
         graph.replay()
         y_pinned.copy_(y_dev, non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = max_over_ranks((time.perf_counter() - w0) / e2e_steps, world, dev)
+    e2e_s = max_over_ranks((time.perf_counter() - w0) / max(1, e2e_steps), world, dev)
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -474,9 +480,9 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": "MMVQ kernel, all launches of the timed step (its one Q8_1 launch "
                                "per case counted in the time)",
                      "achieved_instrumented": round(achieved_instr, 1)},
-        "e2e": {"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
-                "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
-                "steps": e2e_steps},
+        "e2e": ({"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
+                 "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
+                 "steps": e2e_steps} if e2e_steps else None),
         "gpu_launches": (len(calls) + len(case_list)) * args.steps,
         "clocks": clk,
         "cases": per_case,
@@ -647,7 +653,7 @@ def run_moe(args, rank, world, local_rank):
     ratio = profiled_field("mmvq_expert_ffn_moe_t8.md", "traffic_over_weight_bytes")
     traffic = None if ratio is None else round(ratio * float(np.mean(step_bytes)))
 
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = 0 if getattr(args, "light", False) else max(3, min(args.steps, 200))
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     for i in range(e2e_steps):
@@ -657,7 +663,7 @@ def run_moe(args, rank, world, local_rank):
                         y=y, xq=xq, sync=sync, lists=False)
         y_pinned.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = max_over_ranks((time.perf_counter() - w0) / e2e_steps, world, dev)
+    e2e_s = max_over_ranks((time.perf_counter() - w0) / max(1, e2e_steps), world, dev)
     if mmvq.read_device_fault() != 0:
         raise RuntimeError("device fault word set after the timed runs")
     e2e_bytes = metrics.moe_step_bytes(distinct[0], H, F)
@@ -678,10 +684,10 @@ def run_moe(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 3), "traffic": traffic,
                      "algorithmic_bytes_per_launch": round(launch_bytes),
                      "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "mmvq_expert_ffn_kernel"},
-        "e2e": {"value": round(world * e2e_bytes / e2e_s / 1e9, 1), "unit": UNIT,
-                "h2d_bytes_per_step": int(x_host.nbytes + topks[0].nbytes),
-                "d2h_bytes_per_step": int(y.numel() * 4), "steps": e2e_steps,
-                "call": "mmvq.expert_ffn, routing 0 every step"},
+        "e2e": ({"value": round(world * e2e_bytes / e2e_s / 1e9, 1), "unit": UNIT,
+                 "h2d_bytes_per_step": int(x_host.nbytes + topks[0].nbytes),
+                 "d2h_bytes_per_step": int(y.numel() * 4), "steps": e2e_steps,
+                 "call": "mmvq.expert_ffn, routing 0 every step"} if e2e_steps else None),
         "gpu_launches": args.steps,
         "clocks": clk,
         "chain": {"ms_per_step": round(timed["chain"] / args.steps, 4),
@@ -835,6 +841,47 @@ def run_reference(args, rank, world):
     }
 
 
+# --------------------------------------- the other workloads, summarised --
+
+EXTRA_WORKLOADS = ["lm_head", "q4k_dense", "q5k_dense", "moe_t1", "moe_t4", "moe_t8"]
+
+
+def run_extras(args, rank, world, local_rank):
+    """The pages' other matrices, each timed as its own workload (fewer steps,
+    no e2e or CPU leg) and summarised beside the sweep's line: per case
+    us/call chained and dependent, weight GB/s and fraction of measured HBM;
+    per MoE step us/layer for the one-launch layer and the four launches."""
+    import gc
+
+    import torch
+    out = {}
+    for w in EXTRA_WORKLOADS:
+        sub = argparse.Namespace(**vars(args))
+        sub.workload, sub.steps, sub.warmup = w, args.extra_steps, 3
+        sub.no_cpu_baseline, sub.light = True, True
+        if w.startswith("moe_"):
+            r = run_moe(sub, rank, world, local_rank)
+            out[w] = {"workload": WORKLOAD_DESC[w], "us_per_layer": round(r["ms_per_step"] * 1e3, 2),
+                      "weight_gbps": r["value"], "roofline_frac": r["roofline"]["frac"],
+                      "distinct_experts_mean": r["config"]["distinct_experts_mean"],
+                      "four_launches_us_per_layer": round(r["chain"]["ms_per_step"] * 1e3, 2),
+                      "steps": sub.steps, "clocks": r["clocks"]}
+        else:
+            r = run_ours(sub, rank, world, local_rank)
+            out[w] = {"workload": WORKLOAD_DESC[w], "value": r["value"],
+                      "ms_per_step": r["ms_per_step"], "roofline_frac": r["roofline"]["frac"],
+                      "steps": sub.steps, "clocks": r["clocks"],
+                      "cases": [{k: c[k] for k in ("shape", "fmt", "ncols", "us_per_call",
+                                                    "weight_gbps", "frac_of_measured",
+                                                    "us_per_call_dependent",
+                                                    "weight_gbps_dependent")}
+                                for c in r["cases"]]}
+        del r
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_case_for_profile(spec: str, launches: int):
     """One case, launched `launches` times eagerly (for ncu -k/-s/-c captures).
     spec = fmt:ROWSxK:NCOLS, e.g. q6_k_planar:2560x10240:8."""
@@ -868,6 +915,10 @@ def main():
     ap.add_argument("--case", default=None,
                     help="profile mode: launch one case (fmt:ROWSxK:NCOLS) --launches times")
     ap.add_argument("--launches", type=int, default=8)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default workload only: leave out the other workloads' summaries")
+    ap.add_argument("--extra-steps", type=int, default=100,
+                    help="timed steps of each extra workload of the default run")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -897,6 +948,8 @@ def main():
         res = run_prologue(args, rank, world, local_rank)
     else:
         res = run_ours(args, rank, world, local_rank)
+        if args.workload == "q6k_sweep" and not args.no_extra:
+            res["workloads"] = run_extras(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

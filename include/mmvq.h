@@ -148,6 +148,13 @@ MMVQ_API int mmvq_quantize_q8_1(const float* x, int K, int ncols, int64_t ldx, v
  * y: fp32 [ncols][rows].  Requires K % 256 == 0 (PR #1774: the row length a
  * multiple of 256), 1 <= ncols <= 8 (PR #2207: 1 to 8 columns),
  * K <= 16384, 1 <= rows <= 2^31 - 1.
+ * Speed: the GGUF types are a compatibility path for matrices used as
+ * stored (their 2-byte aligned 210-byte Q6_K blocks and 144-byte Q4_K rows
+ * do not stream as whole tiles).  On GB300 they reach about a tenth of HBM
+ * bandwidth against 0.4-0.9 for the planar tiles, so a hot-path caller
+ * repacks once at load with mmvq_repack_planar and passes the *_PLANAR type
+ * (PR #2340 "STRATA_Q6_PLANAR": the head is repacked at load for the same
+ * reason).
  */
 MMVQ_API int mmvq_gemv(int type, const void* W, int64_t rows, int K, const void* xq, int ncols, float* y,
               mmvq_stream_t stream);
@@ -160,7 +167,10 @@ MMVQ_API int mmvq_gemv(int type, const void* W, int64_t rows, int K, const void*
  * previous call is still finishing.  Weights are always streamed before the
  * wait; no kernel of this library that writes weights (repack, gather)
  * lets its successor start early.  Unknown flag bits: MMVQ_ERR_SHAPE.  The
- * flag currently changes the schedule of MMVQ_Q6_K_PLANAR only.
+ * flag changes the schedule of the three planar types (MMVQ_Q4_K_PLANAR,
+ * MMVQ_Q5_K_PLANAR, MMVQ_Q6_K_PLANAR): their activations are staged before
+ * the wait, so the hazard it waives applies to all three.  The GGUF types
+ * (MMVQ_Q4_K, MMVQ_Q6_K) ignore it.
  */
 MMVQ_API int mmvq_gemv_ex(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
                           float* y, unsigned int flags, mmvq_stream_t stream);

@@ -47,18 +47,9 @@ def test_silu_mul_quantize_matches_oracle():
     h_gpu_t = torch.empty((n, F), dtype=torch.float32, device="cuda")
     xq_gpu = host(mmvq.silu_mul_quantize_q8_1(dev(gu), F, h_out=h_gpu_t))
     h_gpu = host(h_gpu_t)
-    xq_orc, h_orc = oracle.silu_mul_quantize(gu, F)
+    _, h_orc = oracle.silu_mul_quantize(gu, F)
     # h within a few ulps (expf on the GPU and the host may differ by an ulp)
     assert np.all(np.abs(h_gpu - h_orc) <= 4e-7 * np.abs(h_orc) + 1e-30)
-    # blocks whose 32 values agree bit for bit must quantise to the same bytes;
-    # elsewhere an ulp of h may move d by one fp16 step and a quant by one
-    same = np.all(h_gpu.reshape(n, F // 32, 32).view(np.uint32) ==
-                  h_orc.reshape(n, F // 32, 32).view(np.uint32), axis=2)
-    assert same.any()
-    assert np.array_equal(xq_gpu[same], xq_orc[same])
-    qg = xq_gpu[~same][:, 4:].view(np.int8).astype(int)
-    qo = xq_orc[~same][:, 4:].view(np.int8).astype(int)
-    assert np.all(np.abs(qg - qo) <= 1)
-    dg = xq_gpu[~same][:, 0:2].copy().view(np.uint16).astype(int)
-    do = xq_orc[~same][:, 0:2].copy().view(np.uint16).astype(int)
-    assert np.all(np.abs(dg - do) <= 1)
+    # the Q8_1 bytes are the oracle's quantisation of the GPU's own h, on
+    # every block: the requantisation adds no rounding of its own
+    assert np.array_equal(xq_gpu, oracle.quantize_q8_1(h_gpu))
