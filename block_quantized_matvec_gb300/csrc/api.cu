@@ -320,13 +320,22 @@ int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, const int
                                     (cudaStream_t)stream);
 }
 
-int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
+int mmvq_launch_shape_ex(int type, int64_t rows, int K, int ncols, int32_t* info, int n_info) {
   if (!dense_type(type)) return MMVQ_ERR_TYPE;
   if (!info) return MMVQ_ERR_NULL;
+  if (n_info < 1) return MMVQ_ERR_SHAPE;
   const int rc = check_weights_shape(rows, K);
   if (rc) return rc;
   if (ncols < 1 || ncols > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
-  return mmvq::dense_shape(type, rows, K, ncols, info);
+  int32_t all[7];
+  const int r2 = mmvq::dense_shape(type, rows, K, ncols, all);
+  if (r2) return r2;
+  for (int i = 0; i < n_info && i < 7; ++i) info[i] = all[i];
+  return MMVQ_OK;
+}
+
+int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info) {
+  return mmvq_launch_shape_ex(type, rows, K, ncols, info, 6);
 }
 
 int mmvq_selftest_wait_timeout(unsigned int limit_us, mmvq_stream_t stream) {

@@ -118,6 +118,36 @@ __device__ __forceinline__ void stage_q8_1(const uint8_t* __restrict__ xq, int K
   }
 }
 
+// stage_q8_1 for a K-slice of the columns: the 32-blocks [kb0, kb0 + Kc/32)
+// of each column (column stride nbq_total blocks) into a staging area laid
+// out as for a K = Kc matrix.  kb0 and Kc are multiples of 8 blocks / 256
+// values, so every source vector is 16-byte aligned.
+__device__ __forceinline__ void stage_q8_1_slice(const uint8_t* __restrict__ xq, int nbq_total,
+                                                 int kb0, int Kc, int ncols, uint8_t* act,
+                                                 float* da, float* sa, int tid, int nthreads) {
+  const int nbq = Kc / kQK8;
+  const int vec_per_col = nbq * 9 / 4;
+  const int rb = act_row_bytes(Kc);
+  for (int c = 0; c < ncols; ++c)
+  for (int vi = tid; vi < vec_per_col; vi += nthreads) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(
+                              xq + ((size_t)c * nbq_total + kb0) * kQ81Bytes) + vi);
+    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int w = 4 * vi + e;
+      const int kb = w / 9;
+      const int k = w - kb * 9;
+      if (k == 0) {
+        da[c * nbq + kb] = half_bits_to_float((uint16_t)(w4[e] & 0xffff));
+        if (sa) sa[c * nbq + kb] = half_bits_to_float((uint16_t)(w4[e] >> 16));
+      } else {
+        *reinterpret_cast<uint32_t*>(act + c * rb + act_off(kb) + 4 * (k - 1)) = w4[e];
+      }
+    }
+  }
+}
+
 // Launches `kern` with programmatic stream serialization allowed, so that
 // it may start while the preceding kernel in the stream drains; every kernel
 // of this library waits (griddepcontrol.wait) before it reads anything the

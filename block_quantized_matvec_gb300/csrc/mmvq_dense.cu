@@ -277,6 +277,7 @@ static int dense_shape_t(int64_t rows, int K, int32_t* info) {
   info[3] = cfg.wr;
   info[4] = cfg.wk;
   info[5] = 0;
+  info[6] = 1;
   return MMVQ_OK;
 }
 

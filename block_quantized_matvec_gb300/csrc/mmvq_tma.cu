@@ -36,29 +36,55 @@
 namespace mmvq {
 
 // Consumers are G groups of P warps (C = G*P); warp C is the producer.  A
-// batch is G of the CTA's row groups (group g takes the g-th); within a
-// batch, stage bb holds, for each group, the P consecutive tiles
-// bb*P .. bb*P+P-1 of its row group, and warp (g, p) takes tile bb*P+p.  The
-// P partial sums of a row group are added in warp order at the batch end.
+// batch is G of the row groups of the CTA's cluster (group g takes the g-th);
+// within a batch, stage bb holds, for each group, the P consecutive tiles
+// bb*P .. bb*P+P-1 of the CTA's K-range of its row group, and warp (g, p)
+// takes tile bb*P+p.  The P partial sums of a row group are added in warp
+// order at the batch end.
+//
+// K-split over a cluster (CS = 2..8 CTAs): CTA rank q of a cluster takes
+// the 256-blocks [q*nb/CS, (q+1)*nb/CS) of every row group of the cluster's
+// batches and stages only those activations, so a matrix with few row groups
+// still covers every SM, and the staged columns take 1/CS of the shared
+// memory.  At each batch end the CTAs of ranks 1..CS-1 write their row sums
+// into rank 0's shared memory (distributed shared memory) and arrive on its
+// `xfull` mbarrier (release at cluster scope); rank 0 adds them in rank order
+// after its own (a fixed order, so results repeat bit for bit) and stores y.
+// The partials are double-buffered by batch parity; before a rank overwrites
+// a buffer two batches on, it waits on its own `xempty` mbarrier, on which
+// rank 0 arrives once it has read that buffer.  Rank 0 arrives only where a
+// later batch will wait, and waits itself for every batch's partials, so no
+// CTA's shared memory is touched by another CTA after it exits.  Every wait
+// is bounded, as the ring's; a cluster barrier is passed once, after the
+// mbarriers are initialised.
 // SUMI: also store every per-32-block integer sum (the parity-debug entry);
 // a separate instance, so the product path carries no per-block test.
-template <int LAYOUT, int NCOLS, bool SUMI>
+// CLUSTER: the cluster instance (CS = cs); the plain instance has CS = 1
+// folded in.
+template <int LAYOUT, int NCOLS, bool SUMI, bool CLUSTER>
 __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t* __restrict__ W,
                                                                int64_t rows, int K,
                                                                const uint8_t* __restrict__ xq,
                                                                float* __restrict__ y,
                                                                int32_t* __restrict__ sumi, int S,
-                                                               int G, int P, uint32_t flags) {
+                                                               int G, int P, int cs,
+                                                               uint32_t flags) {
+  const int CS = CLUSTER ? cs : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int C = G * P;  // consumer warps; warp C produces
   const int nb = K / kQK;
-  const int nbq = K / kQK8;
-  const int rb = act_row_bytes(K);
+  const int nbc = nb / CS;   // 256-blocks of this CTA's K-range
+  const int Kc = K / CS;
+  const int nbq = Kc / kQK8;  // 32-blocks of the K-range (staged)
+  const int rb = act_row_bytes(Kc);
+  const int rank = CLUSTER ? (int)cluster_ctarank() : 0;
+  const int cid = blockIdx.x / CS;  // cluster index (1-D clusters of CS CTAs)
+  const int ncl = gridDim.x / CS;
   const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
   constexpr int TB = tile_bytes(LAYOUT);
-  const int spb = nb / P;  // stages per batch
+  const int spb = nbc / P;  // stages per batch
   const size_t stage_bytes = (size_t)C * TB;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -69,24 +95,36 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   float* da = reinterpret_cast<float*>(act + NCOLS * rb);
   float* sa = da + NCOLS * nbq;  // Q4_K only
   float* red = sa + (has_min(LAYOUT) ? NCOLS * nbq : 0);
+  // cluster exchange: xred [2][CS][G][NCOLS][16] floats (rank 0's is used),
+  // then xfull[2], xempty[2]
+  float* xred = red + C * kMaxCols * kTileRows;
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(xred + (CS > 1 ? 2 * CS * G * NCOLS * kTileRows : 0));
+  uint64_t* xempty = xfull + 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C);
     }
+    if (CLUSTER) {
+      for (int q = 0; q < 2; ++q) {
+        mbar_init(&xfull[q], (CS - 1) * G);
+        mbar_init(&xempty[q], G);
+      }
+    }
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  if (CLUSTER) cluster_sync_all();
   grid_launch_dependents();
 
-  // this CTA's row groups: blockIdx.x, + gridDim.x, ... (row groups < 2^27:
-  // 32-bit divisions, which stay inline)
-  const int64_t my_rgs =
-      (blockIdx.x < n_rg) ? (uint32_t)(n_rg - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  // this cluster's row groups: cid, + ncl, ... (row groups < 2^27: 32-bit
+  // divisions, which stay inline)
+  const int64_t my_rgs = (cid < n_rg) ? (uint32_t)(n_rg - 1 - cid) / ncl + 1 : 0;
   const int64_t batches = (uint32_t)(my_rgs + G - 1) / (uint32_t)G;
   const int64_t total = batches * spb;
+  const int64_t blk0 = (int64_t)rank * nbc;  // first 256-block of the K-range
 
   if (warp == C) {  // ------------------------------------------ producer
     if (lane == 0) {
@@ -106,9 +144,9 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
         const int valid = (int)(left < G ? left : G);
         mbar_expect_tx(&full[slot], (uint32_t)(valid * P * TB));
         for (int g = 0; g < valid; ++g) {
-          const int64_t rg = blockIdx.x + (j * G + g) * (int64_t)gridDim.x;
+          const int64_t rg = cid + (j * G + g) * (int64_t)ncl;
           bulk_g2s(ring + (size_t)slot * stage_bytes + (size_t)g * P * TB,
-                   W + (rg * nb + (int64_t)bb * P) * TB, (uint32_t)(P * TB), &full[slot]);
+                   W + (rg * nb + blk0 + (int64_t)bb * P) * TB, (uint32_t)(P * TB), &full[slot]);
         }
         if (++bb == spb) {
           bb = 0;
@@ -139,8 +177,13 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   const bool stable = (flags & MMVQ_FLAG_XQ_STABLE) != 0;
   bool waited = !stable;
   if (!stable) grid_dependency_wait();
-  stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da,
-             has_min(LAYOUT) ? sa : nullptr, tid, nthreads);
+  if constexpr (!CLUSTER) {
+    stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da,
+               has_min(LAYOUT) ? sa : nullptr, tid, nthreads);
+  } else {
+    stage_q8_1_slice(xq, K / kQK8, (int)blk0 * 8, Kc, NCOLS, act, da,
+                     has_min(LAYOUT) ? sa : nullptr, tid, nthreads);
+  }
   group_sync(1, nthreads);
 
   const int g = warp / P;
@@ -152,9 +195,11 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   for (int64_t j = 0; j < batches; ++j) {
     const int64_t k = j * G + g;
     const bool valid = k < my_rgs;
-    const int64_t rg = blockIdx.x + k * (int64_t)gridDim.x;
+    const int64_t rg = cid + k * (int64_t)ncl;
     const int64_t row = rg * kTileRows + i;
-    int32_t* srow = (SUMI && sumi && valid && row < rows) ? sumi + row * nbq : nullptr;
+    // per-block sums of this row at its global 32-block index
+    int32_t* srow =
+        (SUMI && sumi && valid && row < rows) ? sumi + row * (K / kQK8) + blk0 * 8 : nullptr;
     if (srow && !waited) {
       grid_dependency_wait();
       waited = true;
@@ -173,24 +218,25 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
         par ^= 1u;
       }
       const uint8_t* tile = ring + (size_t)s * stage_bytes + (size_t)warp * TB;
+      const int64_t scs = rows * (K / kQK8);
       if (LAYOUT == kQ4Planar) {
         Q4Half w;
         if (valid) load_q4_tile_smem(tile, lane, w);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q4_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, rows * nbq);
+        if (valid) q4_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
       } else if (LAYOUT == kQ5Planar) {
         Q5Half w;
         if (valid) load_q5_tile_smem(tile, lane, w);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q5_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, rows * nbq);
+        if (valid) q5_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
       } else {
         Q6Half w;
         if (valid) load_q6_tile_smem(tile, lane, w);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, rows * nbq);
+        if (valid) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, scs);
       }
     }
     // halves of each row, then the group's K-slices in warp order
@@ -200,27 +246,88 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
       grid_dependency_wait();
       waited = true;
     }
-    if (P == 1) {
-      if (valid && h == 0 && row < rows) {
+    if constexpr (!CLUSTER) {
+      if (P == 1) {
+        if (valid && h == 0 && row < rows) {
 #pragma unroll
-        for (int c = 0; c < NCOLS; ++c) y[c * rows + row] = acc[c];
+          for (int c = 0; c < NCOLS; ++c) y[c * rows + row] = acc[c];
+        }
+        continue;
       }
-      continue;
-    }
-    if (h == 0) {
+      if (h == 0) {
 #pragma unroll
-      for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
-    }
-    group_sync(2 + g, 32 * P);
-    if (p == 0 && valid && h == 0 && row < rows) {
-#pragma unroll
-      for (int c = 0; c < NCOLS; ++c) {
-        float sum = 0.0f;
-        for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
-        y[c * rows + row] = sum;
+        for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
       }
+      group_sync(2 + g, 32 * P);
+      if (p == 0 && valid && h == 0 && row < rows) {
+#pragma unroll
+        for (int c = 0; c < NCOLS; ++c) {
+          float sum = 0.0f;
+          for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
+          y[c * rows + row] = sum;
+        }
+      }
+      group_sync(2 + g, 32 * P);
+    } else {
+      // this CTA's sum over its P K-slices, then the cluster's K-slices:
+      // ranks 1..CS-1 send, rank 0 adds in rank order
+      float part[NCOLS];
+      if (P == 1) {
+#pragma unroll
+        for (int c = 0; c < NCOLS; ++c) part[c] = acc[c];
+      } else {
+        if (h == 0) {
+#pragma unroll
+          for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
+        }
+        group_sync(2 + g, 32 * P);
+#pragma unroll
+        for (int c = 0; c < NCOLS; ++c) {
+          float sum = 0.0f;
+          if (p == 0 && h == 0)
+            for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
+          part[c] = sum;
+        }
+      }
+      if (p == 0) {
+        const int xb = (int)(j & 1);
+        const uint32_t use = (uint32_t)(j >> 1);
+        float* slot_base = xred + (size_t)xb * CS * G * NCOLS * kTileRows;
+        if (rank != 0) {
+          if (j >= 2 && !*fail && !mbar_wait_cluster(&xempty[xb], (use - 1) & 1u)) {
+            *fail = 1;
+            atomicOr(&g_fault_word, kFaultMbarTimeout);
+          }
+          if (h == 0) {
+            float* mine = slot_base + ((size_t)(rank * G + g) * NCOLS) * kTileRows;
+#pragma unroll
+            for (int c = 0; c < NCOLS; ++c)
+              st_cluster_f32(cluster_map(mine + c * kTileRows + i, 0), part[c]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(cluster_map(&xfull[xb], 0));
+        } else {
+          if (!*fail && !mbar_wait_cluster(&xfull[xb], use & 1u)) {
+            *fail = 1;
+            atomicOr(&g_fault_word, kFaultMbarTimeout);
+          }
+          if (valid && h == 0 && row < rows) {
+#pragma unroll
+            for (int c = 0; c < NCOLS; ++c) {
+              float sum = part[c];
+              for (int q = 1; q < CS; ++q)
+                sum += slot_base[((size_t)(q * G + g) * NCOLS + c) * kTileRows + i];
+              y[c * rows + row] = sum;
+            }
+          }
+          __syncwarp();
+          // the buffer is free again; only where a later batch waits for it
+          if (j + 2 < batches && lane > 0 && lane < CS)
+            mbar_arrive_cluster(cluster_map(&xempty[xb], lane));
+        }
+      }
+      if (P > 1) group_sync(2 + g, 32 * P);
     }
-    group_sync(2 + g, 32 * P);
   }
 }
 
@@ -439,6 +546,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
 struct TmaCfg {
   int G, P, slots, grid;
   size_t smem;
+  int CS;  // CTAs per cluster (K-split); 1: no cluster
 };
 
 // Launch shape.  Candidates (G, P) with P | K/256 and C = G*P <= 12; the ring
@@ -465,14 +573,14 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
       return MMVQ_OK;
     }
   }
-  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false>;
+  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false, false>;
   const int sms = device_sms();
   const size_t limit = max_smem_optin();
   if (sms <= 0 || limit == 0) return MMVQ_ERR_CUDA;
   const int nb = K / kQK;
   const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
   const size_t budget = std::min<size_t>(limit, 110 * 1024);
-  TmaCfg best = {0, 0, 0, 0, 0};
+  TmaCfg best = {0, 0, 0, 0, 0, 1};
   double best_cost = 1e300;
   int best_c = 0;
   // Very tall matrices (an LM head): one warp per row group (no K-split, no
@@ -494,7 +602,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
       // registers allow it, made the one-column head ~6% slower)
       per_sm = std::min(per_sm, 3);
       const int64_t ctas = std::min<int64_t>((n_rg + G - 1) / G, (int64_t)sms * per_sm);
-      best = {G, 1, 2, (int)ctas, smem};
+      best = {G, 1, 2, (int)ctas, smem, 1};
     }
   }
   const bool search = !tall || best.G == 0;
@@ -529,33 +637,111 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
       if (cost < best_cost * 0.999 || (cost < best_cost * 1.001 && G * P > best_c)) {
         best_cost = cost;
         best_c = G * P;
-        best = {G, P, S, (int)ctas, smem};
+        best = {G, P, S, (int)ctas, smem, 1};
       }
     }
   }
   if (best.G == 0) return MMVQ_ERR_SHAPE;
+  // Six to eight columns of a long row (K >= 8192): the staged columns
+  // (>= 72 KB) leave the ring two stages and one CTA per SM, and a matrix of
+  // few row groups covers part of the GPU (2560 x 10240: 80 CTAs).  A K-split
+  // over CTA pairs halves the staging and spreads each row group over two
+  // SMs: three row groups of four K-slices per CTA.  Measured on GB300 for
+  // 2560 x 10240 at 6 / 8 columns: 18.4 / 19.5 -> 13.1 / 14.5 us as a
+  // dependent chain, 10.1 / 10.9 -> 9.9 / 11.0 us back to back.
+  if (NCOLS >= 6 && nb >= 32 && (nb / 2) % 4 == 0 && best.grid < sms) {
+    auto ckern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false, true>;
+    const int G = 3, P = 4, CS = 2;
+    int S = 0;
+    size_t smem = 0;
+    for (int s = 32; s >= 2; --s) {
+      const size_t b = tma_smem_bytes(LAYOUT, s, K, NCOLS, G, P, CS);
+      if (b <= budget || (s == 2 && b <= limit)) {
+        S = s;
+        smem = b;
+        break;
+      }
+    }
+    if (S >= 2) {
+      if (ensure_smem((const void*)ckern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
+      cudaLaunchConfig_t lc = {};
+      lc.blockDim = dim3(32 * (G * P + 1));
+      lc.gridDim = dim3(2 * sms);
+      lc.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = CS;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      lc.attrs = attr;
+      lc.numAttrs = 1;
+      int max_cl = 0;
+      if (cudaOccupancyMaxActiveClusters(&max_cl, (void*)ckern, &lc) == cudaSuccess && max_cl >= 1) {
+        const int64_t n_batch = (n_rg + G - 1) / G;
+        const int64_t ncl = std::min<int64_t>(n_batch, max_cl);
+        best = {G, P, S, (int)(ncl * CS), smem, CS};
+      }
+    }
+  }
   std::lock_guard<std::mutex> lock(mu);
   cache[key] = best;
   *out = best;
   return MMVQ_OK;
 }
 
+// A launch shape the kernel can run: a ring of at least two stages, at most
+// 12 consumer warps, CS | K/256 and P | (K/256)/CS, a grid of whole clusters
+// of 1-8 CTAs, and the shared memory the shape needs.
+static bool tma_shape_ok(const TmaCfg& c, int K, int layout, int ncols) {
+  const int nb = K / kQK;
+  if (c.slots < 2 || c.G < 1 || c.P < 1 || c.G * c.P > 12) return false;
+  if (c.CS < 1 || c.CS > 8) return false;
+  if (nb % c.CS != 0 || (nb / c.CS) % c.P != 0 || c.grid < c.CS || c.grid % c.CS != 0) return false;
+  return c.smem >= tma_smem_bytes(layout, c.slots, K, ncols, c.G, c.P, c.CS) &&
+         c.smem <= max_smem_optin();
+}
+
 // The instance that also stores the per-block sums runs in the product
 // instance's launch shape, so y comes out with the same bits.
+template <int LAYOUT, int NCOLS, bool SUMI>
+static int launch_tma_cfg(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
+                          int32_t* sumi, const TmaCfg& cfg, uint32_t flags, cudaStream_t stream) {
+  if (!tma_shape_ok(cfg, K, LAYOUT, NCOLS)) return MMVQ_ERR_SHAPE;
+  if (cfg.CS == 1) {
+    auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, false>;
+    if (ensure_smem((const void*)kern, cfg.smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
+    return launch_pdl(kern, dim3(cfg.grid), dim3(32 * (cfg.G * cfg.P + 1)), cfg.smem, stream, W,
+                      rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, 1, flags);
+  }
+  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, true>;
+  if (ensure_smem((const void*)kern, cfg.smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(cfg.grid);
+  lc.blockDim = dim3(32 * (cfg.G * cfg.P + 1));
+  lc.dynamicSmemBytes = cfg.smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cfg.CS;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  return cudaLaunchKernelEx(&lc, kern, W, rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, cfg.CS,
+                            flags) == cudaSuccess
+             ? MMVQ_OK
+             : MMVQ_ERR_CUDA;
+}
+
 template <int LAYOUT, int NCOLS, bool SUMI>
 static int launch_tma_s(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
                         int32_t* sumi, uint32_t flags, cudaStream_t stream) {
   TmaCfg cfg;
   const int rc = tma_config<LAYOUT, NCOLS>(rows, K, &cfg);
   if (rc != MMVQ_OK) return rc;
-  // the ring needs at least two stages (the chooser never picks fewer)
-  if (cfg.slots < 2 || cfg.G < 1 || cfg.P < 1 || cfg.G * cfg.P > 12) return MMVQ_ERR_SHAPE;
-  if (SUMI &&
-      ensure_smem((const void*)mmvq_planar_tma_kernel<LAYOUT, NCOLS, true>, cfg.smem) != MMVQ_OK)
-    return MMVQ_ERR_CUDA;
-  return launch_pdl(mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI>, dim3(cfg.grid),
-                    dim3(32 * (cfg.G * cfg.P + 1)), cfg.smem, stream, W, rows, K, xq, y, sumi,
-                    cfg.slots, cfg.G, cfg.P, flags);
+  return launch_tma_cfg<LAYOUT, NCOLS, SUMI>(W, rows, K, xq, y, sumi, cfg, flags, stream);
 }
 
 template <int LAYOUT, int NCOLS>
@@ -592,6 +778,43 @@ int launch_planar_tma(int type, const void* W, int64_t rows, int K, const void* 
   return launch_tma_layout<kQ6Planar>(w, rows, K, x, ncols, y, sumi, flags, s);
 }
 
+template <int LAYOUT>
+static int launch_tma_cfg_l(const uint8_t* w, int64_t rows, int K, const uint8_t* x, int ncols,
+                            float* y, int32_t* sumi, const TmaCfg& c, uint32_t flags,
+                            cudaStream_t s) {
+#define MMVQ_TC(N)                                                                         \
+  return sumi ? launch_tma_cfg<LAYOUT, N, true>(w, rows, K, x, y, sumi, c, flags, s)     \
+              : launch_tma_cfg<LAYOUT, N, false>(w, rows, K, x, y, sumi, c, flags, s)
+  switch (ncols) {
+    case 1: MMVQ_TC(1);
+    case 2: MMVQ_TC(2);
+    case 3: MMVQ_TC(3);
+    case 4: MMVQ_TC(4);
+    case 5: MMVQ_TC(5);
+    case 6: MMVQ_TC(6);
+    case 7: MMVQ_TC(7);
+    case 8: MMVQ_TC(8);
+  }
+#undef MMVQ_TC
+  return MMVQ_ERR_NCOLS;
+}
+
+// The ring kernel in an explicit launch shape (G, P, stages, CS, grid), with
+// the shared memory the shape needs; the shape is checked as the chooser's.
+int launch_planar_tma_shape(int type, const void* W, int64_t rows, int K, const void* xq,
+                            int ncols, float* y, int32_t* sumi, int G, int P, int S, int CS,
+                            int grid, uint32_t flags, cudaStream_t s) {
+  const int layout =
+      type == MMVQ_Q4_K_PLANAR ? kQ4Planar : type == MMVQ_Q5_K_PLANAR ? kQ5Planar : kQ6Planar;
+  if (G < 1 || P < 1 || S < 2 || CS < 1 || CS > 8) return MMVQ_ERR_SHAPE;
+  TmaCfg c = {G, P, S, grid, tma_smem_bytes(layout, S, K, ncols, G, P, CS), CS};
+  const uint8_t* w = static_cast<const uint8_t*>(W);
+  const uint8_t* x = static_cast<const uint8_t*>(xq);
+  if (layout == kQ4Planar) return launch_tma_cfg_l<kQ4Planar>(w, rows, K, x, ncols, y, sumi, c, flags, s);
+  if (layout == kQ5Planar) return launch_tma_cfg_l<kQ5Planar>(w, rows, K, x, ncols, y, sumi, c, flags, s);
+  return launch_tma_cfg_l<kQ6Planar>(w, rows, K, x, ncols, y, sumi, c, flags, s);
+}
+
 template <int LAYOUT, int NCOLS>
 static int tma_shape_t(int64_t rows, int K, int32_t* info) {
   TmaCfg cfg;
@@ -603,6 +826,7 @@ static int tma_shape_t(int64_t rows, int K, int32_t* info) {
   info[3] = cfg.G;
   info[4] = cfg.P;
   info[5] = cfg.slots;
+  info[6] = cfg.CS;
   return MMVQ_OK;
 }
 

@@ -77,6 +77,63 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---- thread-block clusters (the dense kernel's K-split over CTAs) ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The shared::cluster address of `p` (a shared variable of this CTA) in
+// the CTA of the cluster with the given rank.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Arrival on an mbarrier of another CTA of the cluster; release at cluster
+// scope, so this thread's earlier stores into that CTA are visible to a
+// thread whose wait observes the phase.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait with acquire at cluster scope (arrivals from other CTAs).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      const uint64_t t = global_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > limit_ns) {
+        return false;
+      }
+    }
+  }
+}
+// All threads of every CTA of the cluster (used once, after the mbarriers
+// are initialised and before any CTA touches another's shared memory).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
 // Tile bytes of lane L out of a ring slot: the same offsets as in global
 // memory, so each warp-wide 16-byte load covers 512 consecutive bytes.
 __device__ __forceinline__ void load_q6_tile_smem(const uint8_t* tile, int lane, Q6Half& w) {
@@ -114,11 +171,17 @@ __host__ __device__ constexpr bool has_min(int layout) {
 __host__ __device__ constexpr int tile_bytes(int layout) {
   return layout == kQ4Planar ? kTileBytesQ4 : layout == kQ5Planar ? kTileBytesQ5 : kTileBytes;
 }
-__host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int ncols, int G, int P) {
+// With a K-split over a cluster of CS CTAs each stages K/CS of the
+// activations and holds the exchange buffers [2][CS][G][ncols][16] floats
+// and two pairs of mbarriers.
+__host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int ncols, int G, int P,
+                                                 int CS = 1) {
   const int C = G * P;
-  return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + (size_t)ncols * act_row_bytes(K) +
-         (size_t)ncols * (K / kQK8) * 4 * (has_min(layout) ? 2 : 1) +
-         (size_t)C * kMaxCols * kTileRows * 4;
+  const int Kc = K / CS;
+  return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + (size_t)ncols * act_row_bytes(Kc) +
+         (size_t)ncols * (Kc / kQK8) * 4 * (has_min(layout) ? 2 : 1) +
+         (size_t)C * kMaxCols * kTileRows * 4 +
+         (CS > 1 ? (size_t)2 * CS * G * ncols * kTileRows * 4 + 32 : 0);
 }
 
 __device__ __forceinline__ void group_sync(int id, int nthreads) {

@@ -53,6 +53,7 @@ SIGNATURES = {
     "mmvq_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "mmvq_rmsnorm_quantize_q8_1": (_I, [_P, _P, ctypes.c_float, _I, _I, _I64, _P, _P, _P]),
     "mmvq_launch_shape": (_I, [_I, _I64, _I, _I, _P]),
+    "mmvq_launch_shape_ex": (_I, [_I, _I64, _I, _I, _P, _I]),
     "mmvq_expert_ffn": (_I, [_I, _P, _P, _I, _I, _I, _P, _I64, _I, _P, _I, _P, _P, _P, _P, _P,
                              _P, _P, _P, _P, _P, _P]),
     "mmvq_expert_ffn_noalloc": (_I, [_I, _P, _P, _I, _I, _I, _P, _I64, _I, _P, _I, _P, _P, _P,
@@ -334,11 +335,11 @@ def silu_mul_quantize_q8_1(gu: torch.Tensor, F: int, out: torch.Tensor | None = 
 
 def launch_shape(type_: int, rows: int, K: int, ncols: int) -> dict:
     """The launch shape mmvq_gemv picks (host-only query)."""
-    info = (ctypes.c_int32 * 6)()
-    _check(lib().mmvq_launch_shape(type_, rows, K, ncols, info), "mmvq_launch_shape")
-    keys = (["grid", "threads", "smem", "G", "P", "stages"]
+    info = (ctypes.c_int32 * 7)()
+    _check(lib().mmvq_launch_shape_ex(type_, rows, K, ncols, info, 7), "mmvq_launch_shape_ex")
+    keys = (["grid", "threads", "smem", "G", "P", "stages", "cluster"]
             if type_ in (TYPE_Q6_K_PLANAR, TYPE_Q4_K_PLANAR, TYPE_Q5_K_PLANAR)
-            else ["grid", "threads", "smem", "WR", "WK", "unused"])
+            else ["grid", "threads", "smem", "WR", "WK", "unused", "cluster"])
     return dict(zip(keys, list(info)))
 
 

@@ -392,6 +392,16 @@ MMVQ_API int mmvq_gather_planar_rows(const void* W_planar, int64_t rows, int K, 
 MMVQ_API int mmvq_launch_shape(int type, int64_t rows, int K, int ncols, int32_t* info);
 
 /*
+ * mmvq_launch_shape writing n_info (1..7) values; the seventh is the
+ * number of CTAs per thread-block cluster of the planar kernel (1: no
+ * cluster; 2: each row group's K split over a pair of CTAs that add their
+ * partial sums through distributed shared memory).  No counterpart on the
+ * pages.
+ */
+MMVQ_API int mmvq_launch_shape_ex(int type, int64_t rows, int K, int ncols, int32_t* info,
+                                  int n_info);
+
+/*
  * Device fault word of the bulk-copy kernels.  Every wait of those kernels
  * on a shared-memory barrier, and of mmvq_expert_ffn on its grid barriers,
  * is bounded (about one second); a wait that runs out sets a bit here (1: a

@@ -105,3 +105,30 @@ def test_output_rows_outside_the_matrix_are_untouched():
     out = canary[:2 * rows].view(2, rows)
     mmvq.gemv(t_gpu, Wd, rows, K, xqd, 2, out=out)
     assert np.all(host(canary[2 * rows:]) == 12345.0)
+
+
+@pytest.mark.parametrize("kind", list(KINDS))
+@pytest.mark.parametrize("rows,K,ncols", [(2560, 10240, 8), (2560, 10240, 6), (33, 10240, 7),
+                                          (5, 16384, 8)])
+def test_cluster_k_split_exact_sums_and_repeatable(kind, rows, K, ncols):
+    # six to eight columns of a long row run with each row group's K split
+    # over a pair of CTAs (partials added through distributed shared memory)
+    if kind.endswith("_planar"):
+        t = KINDS[kind][0]
+        assert mmvq.launch_shape(t, rows, K, ncols)["cluster"] == 2
+    salt = rows + K + ncols
+    W, Wd, t_gpu, t_orc = _weights(kind, rows, K, salt)
+    x = synth.activations(K, ncols, salt=salt)
+    xq = oracle.quantize_q8_1(x)
+    xqd = mmvq.quantize_q8_1(dev(x))
+    sel = np.unique(np.linspace(0, rows - 1, min(rows, 64)).astype(np.int64))
+    sumi, y_dbg = mmvq.debug_block_sums(t_gpu, Wd, rows, K, xqd, ncols)
+    s_ref = oracle.block_sums(t_orc, np.ascontiguousarray(W[sel]), sel.size, K, xq, ncols)
+    assert np.array_equal(host(sumi)[:, sel], s_ref)
+    runs = [host(mmvq.gemv(t_gpu, Wd, rows, K, xqd, ncols)) for _ in range(3)]
+    for r in runs[1:]:
+        assert np.array_equal(r.view(np.uint32), runs[0].view(np.uint32))
+    assert np.array_equal(runs[0].view(np.uint32), host(y_dbg).view(np.uint32))
+    y_ref, bound = oracle.gemv(t_orc, np.ascontiguousarray(W[sel]), sel.size, K, xq, ncols,
+                               with_bound=True)
+    assert_within_bound(runs[0][:, sel], y_ref, bound, f"{kind} {rows}x{K} ncols={ncols}")
