@@ -12,17 +12,24 @@
 //  - Every CTA builds the token lists itself, in shared memory, from topk
 //    (a few hundred slots at most), so its producer starts the gate|up
 //    weight stream at once; CTA 0 also publishes the lists.
-//  - The T <= 8 hidden states are quantised to Q8_1 by all consumer warps of
-//    the grid, one 32-block each, into the caller's xq; a CTA stages a
-//    group's columns from there (through L2) when the group changes.
+//  - One or two tokens: every CTA quantises the hidden states itself into
+//    its own staging, one 32-block per four lanes (values loaded by volatile
+//    loads at entry, so they arrive before the CTA's weight stream starts;
+//    the division done as a checked reciprocal multiply with the same bytes
+//    as the IEEE quotient), so no grid barrier precedes gate|up; CTA 0 also
+//    writes xq.  Three or more tokens: the hidden states are quantised to
+//    Q8_1 by all consumer warps of the grid, one 32-block each, into the
+//    caller's xq, behind a grid barrier; a CTA stages a group's columns from
+//    there (through L2) when the group changes.
 //  - The producer streams the CTA's gate|up items and then, through the same
 //    ring, its down items: the down weights are in flight while the
 //    consumers finish gate|up and wait at the grid barriers.
 //  - Grid barriers over the consumer threads: after the Q8_1 of the hidden
-//    states, and after gate|up (every row of every position written).  One
-//    or two tokens: a CTA then requantises the SiLU*up of its down columns
-//    itself while staging them.  Three or more: all consumer warps of the
-//    grid share SiLU*up -> Q8_1 out block by block, behind a third barrier.
+//    states (three or more tokens), and after gate|up (every row of every
+//    position written).  One or two tokens: a CTA then requantises the
+//    SiLU*up of its down columns itself while staging them.  Three or more:
+//    all consumer warps of the grid share SiLU*up -> Q8_1 out block by block,
+//    behind a third barrier.
 //    The producer does not wait at them.
 // Items, shares and the consume routine are those of the grouped kernel: an
 // item is G row groups of one non-empty group's expert, each CTA takes an
@@ -57,11 +64,14 @@ constexpr int kFfnMaxSlots = 256;
 // Shared memory of a CTA with C consumer warps: the ring (S stages of C
 // tiles), one group's staged columns (CM x max(H, F) quants, d and s), the
 // K-slice partials.
+// One or two tokens (CM <= 2) add the CTA's own Q8_1 of the hidden states
+// (CM x act_row_bytes(H) quants, d and s).
 __host__ __device__ inline size_t ffn_smem_bytes(int layout, int S, int H, int F, int CM, int C) {
   const int Km = H > F ? H : F;
   return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) +
          (size_t)CM * act_row_bytes(Km) + (size_t)CM * (Km / kQK8) * 8 +
-         (size_t)C * kMaxCols * kTileRows * 4;
+         (size_t)C * kMaxCols * kTileRows * 4 +
+         (CM <= 2 ? (size_t)CM * act_row_bytes(H) + (size_t)CM * (H / kQK8) * 8 : 0);
 }
 
 // The counter's top bit as a barrier finds it: read once per CTA before the
@@ -254,6 +264,11 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
   float* da = reinterpret_cast<float*>(act + (size_t)CM * act_row_bytes(Km));
   float* sa = da + CM * (Km / kQK8);
   float* red = sa + CM * (Km / kQK8);
+  // T <= 2: the CTA's own Q8_1 of the hidden states, [T][act_row_bytes(H)]
+  // quants, then d and s as floats [T][H/32] each
+  uint8_t* xact = reinterpret_cast<uint8_t*>(red + C * kMaxCols * kTileRows);
+  float* xda = reinterpret_cast<float*>(xact + (size_t)(CM <= 2 ? CM : 0) * act_row_bytes(H));
+  float* xsa = xda + (CM <= 2 ? CM : 0) * nbq_h;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -267,15 +282,35 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
   // the barrier word's top bit, as left by earlier launches (read now, used
   // at the first barrier)
   uint32_t phase = grid_barrier_phase(a.sync);
-  // each consumer warp's first hidden-state value (at most one 32-block per
-  // warp for T <= 8 on a full GPU), loaded now so the load overlaps the lists
   const int gwarp = blockIdx.x * C + warp;  // this warp's index in the grid
   const int nwarps = gridDim.x * C;
   const int n_xblk = a.T * nbq_h;
+  // The hidden-state values, loaded now (volatile loads, issued here) so
+  // that they arrive before the CTA's weight stream starts.  T <= 2: every
+  // CTA quantises all of them itself, one 32-block per consumer thread
+  // (16-byte loads when x allows them), so no grid barrier comes before
+  // gate|up.  Otherwise each consumer warp of the grid takes one 32-block
+  // (at most one per warp for T <= 8 on a full GPU).
   float x_first = 0.0f;
-  if (warp < C && gwarp < n_xblk) {
-    const int t = gwarp / nbq_h;
-    x_first = a.x[(int64_t)t * a.ldx + (gwarp - t * nbq_h) * kQK8 + lane];
+  float4 xr[CM <= 2 ? 2 : 1];
+  const bool x_vec = ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) && (a.ldx % 4 == 0);
+  if constexpr (CM <= 2) {
+    // quad q = threadIdx.x / 4 takes block q, its lane j values 8j .. 8j+7
+    const int blk = threadIdx.x >> 2;
+    if (threadIdx.x < 32 * C && blk < n_xblk && x_vec) {
+      const int t = blk / nbq_h;
+      const float* src = a.x + (int64_t)t * a.ldx + (blk - t * nbq_h) * kQK8 + 8 * (lane & 3);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(xr[i].x), "=f"(xr[i].y), "=f"(xr[i].z), "=f"(xr[i].w)
+                     : "l"(src + 4 * i));
+    }
+  } else {
+    if (warp < C && gwarp < n_xblk) {
+      const int t = gwarp / nbq_h;
+      x_first = a.x[(int64_t)t * a.ldx + (gwarp - t * nbq_h) * kQK8 + lane];
+    }
   }
 
   // 1. token lists, in shared memory (every CTA; CTA 0 reports bad ids)
@@ -339,21 +374,78 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
   const int nthreads = 32 * C;
   int slot = 0;
   uint32_t par = 0;
-  // 4. the T hidden states as Q8_1, one 32-block per warp of the grid
-  for (int blk = gwarp; blk < n_xblk; blk += nwarps) {
-    const int t = blk / nbq_h;
-    const int kb = blk - t * nbq_h;
-    const float v = blk == gwarp ? x_first : a.x[(int64_t)t * a.ldx + kb * kQK8 + lane];
-    quantize_lane(v, a.xq + (size_t)blk * kQ81Bytes, lane);
-  }
-  if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs, phase) &&
-      threadIdx.x == 0)
-    atomicOr(&g_fault_word, kFaultGridBarrier);
-  // 5. gate|up: a group's columns are its tokens' hidden states
   const uint8_t* xq = a.xq;
+  if constexpr (CM <= 2) {
+    // 4. one or two tokens: the CTA quantises the T hidden states into its
+    // own staging, a 32-block per quad of lanes (CTA 0 also writes xq); the
+    // bytes are those of the plain quantiser
+    const int nquads = nthreads / 4;
+    for (int blk0 = 0; blk0 < n_xblk; blk0 += nquads) {
+      const int blk = blk0 + (int)(threadIdx.x >> 2);
+      const bool on = blk < n_xblk;
+      const int j = lane & 3;
+      const int t = on ? blk / nbq_h : 0;
+      const int kb = on ? blk - t * nbq_h : 0;
+      float v[8];
+      if (on && blk0 == 0 && x_vec) {
+        v[0] = xr[0].x; v[1] = xr[0].y; v[2] = xr[0].z; v[3] = xr[0].w;
+        v[4] = xr[1].x; v[5] = xr[1].y; v[6] = xr[1].z; v[7] = xr[1].w;
+      } else {
+        const float* src = a.x + (int64_t)t * a.ldx + kb * kQK8 + 8 * j;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = on ? src[i] : 0.0f;
+      }
+      uint32_t w0, w1, header;
+      quantize_block_quad(v, w0, w1, header);
+      if (on) {
+        *reinterpret_cast<uint2*>(xact + (size_t)t * act_row_bytes(H) + act_off(kb) + 8 * j) =
+            make_uint2(w0, w1);
+        if (j == 0) {
+          xda[t * nbq_h + kb] = half_bits_to_float((uint16_t)(header & 0xffffu));
+          if (has_min(LAYOUT)) xsa[t * nbq_h + kb] = half_bits_to_float((uint16_t)(header >> 16));
+        }
+        if (blockIdx.x == 0) {
+          uint32_t* o = reinterpret_cast<uint32_t*>(a.xq + (size_t)blk * kQ81Bytes);
+          if (j == 0) o[0] = header;
+          o[1 + 2 * j] = w0;
+          o[2 + 2 * j] = w1;
+        }
+      }
+    }
+    group_sync(1, nthreads);
+  } else {
+    // 4. the T hidden states as Q8_1, one 32-block per warp of the grid
+    for (int blk = gwarp; blk < n_xblk; blk += nwarps) {
+      const int t = blk / nbq_h;
+      const int kb = blk - t * nbq_h;
+      const float v = blk == gwarp ? x_first : a.x[(int64_t)t * a.ldx + kb * kQK8 + lane];
+      quantize_lane(v, a.xq + (size_t)blk * kQ81Bytes, lane);
+    }
+    if (!grid_barrier_bounded(a.sync, gridDim.x, nthreads, &ok_s, kWaitLimitNs, phase) &&
+        threadIdx.x == 0)
+      atomicOr(&g_fault_word, kFaultGridBarrier);
+  }
+  // 5. gate|up: a group's columns are its tokens' hidden states (copied from
+  // the CTA's own staging for T <= 2, else staged from xq through L2)
   auto stage_gu = [=](int p0, int n, bool) {
-    stage_q8_1<true>(xq, H, n, [=](int c) { return tok_s[p0 + c]; }, act, da,
-                     has_min(LAYOUT) ? sa : nullptr, threadIdx.x, nthreads);
+    if constexpr (CM <= 2) {
+      // the chunk layout of the gate|up phase (K = H): rows of
+      // act_row_bytes(H), d and s at [c][H/32]
+      const int rbh = act_row_bytes(H);
+      for (int c = 0; c < n; ++c) {
+        const int t = tok_s[p0 + c];
+        const uint4* src = reinterpret_cast<const uint4*>(xact + (size_t)t * rbh);
+        uint4* dst = reinterpret_cast<uint4*>(act + (size_t)c * rbh);
+        for (int v = threadIdx.x; v < rbh / 16; v += nthreads) dst[v] = src[v];
+        for (int v = threadIdx.x; v < nbq_h; v += nthreads) {
+          da[c * nbq_h + v] = xda[t * nbq_h + v];
+          if (has_min(LAYOUT)) sa[c * nbq_h + v] = xsa[t * nbq_h + v];
+        }
+      }
+    } else {
+      stage_q8_1<true>(xq, H, n, [=](int c) { return tok_s[p0 + c]; }, act, da,
+                       has_min(LAYOUT) ? sa : nullptr, threadIdx.x, nthreads);
+    }
   };
   ffn_consume<LAYOUT, CM>(r, slot, par, warp, lane, nthreads, a.g_gu, a.p_gu, H, nrg_gu, nrgb_gu,
                           i0, i1, active, offs_s, act, da, sa, red, a.gu, 2 * F, stage_gu);

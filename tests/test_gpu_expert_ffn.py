@@ -275,3 +275,43 @@ def test_grid_barrier_timeout_is_reported_without_a_fault():
     assert mmvq.read_device_fault() & 2
     # the context stays usable: a full call afterwards is correct
     _check_synthetic("q4_k_planar", 8, 256, 256, 2, 2, salt=3)
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_hidden_state_quantisation_at_ties_bit_exact(T):
+    # one or two tokens: every CTA quantises the hidden states itself, a block
+    # per thread, with a reciprocal-multiply candidate checked against the
+    # exact quotient; values whose quotient x/d sits exactly on, or one ulp
+    # either side of, a half-integer must give the plain definition's bytes
+    E, H, F, k = 8, 512, 256, 2
+    rng = np.random.default_rng(31 + T)
+    x = np.zeros((T, H), np.float32)
+    for t in range(T):
+        for b in range(H // 32):
+            blk = np.zeros(32, np.float32)
+            kind = b % 4
+            if kind == 0:                                   # d = 1: exact ties k + 0.5
+                blk[:] = np.arange(32) - 15.5
+                blk[0] = 127.0
+            elif kind == 1:                                 # one ulp either side of the ties
+                base = (np.arange(32) - 15.5).astype(np.float32)
+                away = np.where(rng.random(32) < 0.5, -200.0, 200.0).astype(np.float32)
+                blk[:] = np.nextafter(base, away)
+                blk[0] = 127.0
+            elif kind == 2:                                 # d not a power of two, ties in x/d
+                amax = np.float32(rng.uniform(0.5, 4.0))
+                d = np.float32(amax / np.float32(127.0))
+                m = rng.integers(-126, 126, 32)
+                blk[:] = ((m + 0.5) * d).astype(np.float32)
+                blk[0] = amax
+            else:                                           # plain random values
+                blk[:] = rng.standard_normal(32).astype(np.float32) * np.float32(0.02)
+            x[t, 32 * b:32 * b + 32] = blk
+    W_gu = synth.expert_weights("q4_k", E, 2 * F, H, salt=T)
+    W_dn = synth.expert_weights("q4_k", E, H, F, salt=T + 1)
+    topk = synth.routing(T, k, E, salt=T)
+    got, _ = _run("q4_k_planar", W_gu, W_dn, E, H, F, x, topk)
+    assert np.array_equal(got["xq"], oracle.quantize_q8_1(x))
+    ref = _oracle_chain("q4_k_planar", W_gu, W_dn, E, H, F, x, topk)
+    n = T * k
+    assert_within_bound(got["gu"][:n], ref["gu"], ref["gu_bound"], f"gate|up T={T}")
