@@ -650,7 +650,7 @@ def run_moe(args, rank, world, local_rank):
     achieved = launch_bytes / (fused_ms * 1e-3 / args.steps) / 1e9
     # DRAM bytes per launch: the profiled traffic / weight-byte ratio (T=8
     # capture) applied to this run's mean weight bytes
-    ratio = profiled_field("mmvq_expert_ffn_moe_t8.md", "traffic_over_weight_bytes")
+    ratio = profiled_field("mmvq_expert_ffn_moe_t1_t8.md", "traffic_over_weight_bytes")
     traffic = None if ratio is None else round(ratio * float(np.mean(step_bytes)))
 
     e2e_steps = 0 if getattr(args, "light", False) else max(3, min(args.steps, 200))
@@ -903,6 +903,47 @@ def run_case_for_profile(spec: str, launches: int):
     print(json.dumps({"case": spec, "launches": launches, "y0": float(y[0, 0])}))
 
 
+def run_moe_case_for_profile(spec: str, launches: int):
+    """The bench's MoE layer launched eagerly `launches` times (routings 100, 101,
+    ...), for ncu captures.  spec = moe:T (the one-launch layer) or moe4:T (the
+    same step as four launches)."""
+    import torch
+    from block_quantized_matvec_gb300 import mmvq, synth
+    kind, T = spec.split(":")
+    T = int(T)
+    E, H, F, k = MOE["experts"], MOE["hidden"], MOE["ffn"], MOE["top_k"]
+    dev = torch.device("cuda")
+    q4 = mmvq.TYPE_Q4_K
+
+    def planar(rows, K, salt):
+        host = synth.expert_weights("q4_k", E, rows, K, salt=salt)
+        per = mmvq.planar_bytes(rows, K, q4)
+        out = torch.empty(E * per, dtype=torch.uint8, device=dev)
+        for e in range(E):
+            mmvq.repack_planar(torch.from_numpy(host[e].reshape(-1)).to(dev), rows, K,
+                               out=out[e * per:(e + 1) * per], type_=q4)
+        return out
+
+    W_gu, W_dn = planar(2 * F, H, 1), planar(H, F, 2)
+    x = torch.from_numpy(synth.moe_hidden(H, T)).to(dev)
+    sync = mmvq.expert_ffn_workspace(dev)
+    n = T * k
+    for r in range(launches):
+        topk = torch.from_numpy(synth.routing(T, k, E, salt=100 + r)).to(dev)
+        if kind == "moe":
+            mmvq.expert_ffn(mmvq.TYPE_Q4_K_PLANAR, W_gu, W_dn, E, H, F, x, topk, lists=False,
+                            sync=sync)
+        else:
+            xq, eids, offs, act, _, st = mmvq.quantize_route_groups(x, topk, E)
+            gu = mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_gu, E, 2 * F, H, eids, offs, act, xq, T, n,
+                              status=st)
+            hq = mmvq.silu_mul_quantize_q8_1(gu, F)
+            mmvq.grouped(mmvq.TYPE_Q4_K_PLANAR, W_dn, E, H, F, eids, offs, None, hq, n, n,
+                         status=st)
+    torch.cuda.synchronize()
+    print(json.dumps({"case": spec, "launches": launches}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -913,7 +954,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="profile mode: launch one case (fmt:ROWSxK:NCOLS) --launches times")
+                    help="profile mode: launch one case (fmt:ROWSxK:NCOLS, or moe:T / moe4:T for "
+                         "the MoE layer in one / four launches) --launches times")
     ap.add_argument("--launches", type=int, default=8)
     ap.add_argument("--no-extra", action="store_true",
                     help="default workload only: leave out the other workloads' summaries")
@@ -924,7 +966,10 @@ def main():
         ap.error("--warmup must be >= 3")
 
     if args.case:
-        run_case_for_profile(args.case, args.launches)
+        if args.case.startswith("moe"):
+            run_moe_case_for_profile(args.case, args.launches)
+        else:
+            run_case_for_profile(args.case, args.launches)
         return
 
     rank = int(os.environ.get("RANK", "0"))
