@@ -21,8 +21,10 @@ from pinned host memory and all outputs read back every step.
 
 The default run also times the pages' other matrices (the LM head and the
 gathered draft head at 1-5 columns, the Q4_K and Q5_K dense shapes, the MoE
-layer at T = 1, 4, 8), each as its own workload with fewer steps, and adds
-their summaries under `workloads` (`--no-extra` leaves them out).
+layer at T = 1, 4, 8), each as its own workload with fewer steps, and
+one-column decode steps as a dependent chain (quantiser + product against
+the fused fp32 entry), and adds their summaries under `workloads`
+(`--no-extra` leaves them out).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a row sample
@@ -841,6 +843,89 @@ def run_reference(args, rank, world):
     }
 
 
+# ------------------------------------------------ one-column decode steps --
+
+DECODE_SHAPES = [("q6_k_planar", 2560, 2560), ("q6_k_planar", 2560, 10240),
+                 ("q6_k_planar", 10240, 2560), ("q4_k_planar", 12288, 2560),
+                 ("q6_k_planar", HEAD_SHAPE[0], HEAD_SHAPE[1])]
+
+
+def run_decode(args, rank, world, local_rank):
+    """One decode step per matrix: an fp32 column in, y out, each step waiting
+    for the previous one (a dependent chain over rotating weight copies > 2x
+    L2).  Two ways, timed as CUDA graphs of the same steps: the quantiser and
+    the product as two launches (mmvq_quantize_q8_1, mmvq_gemv), and
+    mmvq_gemv_f32 (one launch where the CTAs quantise the column themselves).
+    us per step and weight GB/s for each."""
+    import torch
+    from block_quantized_matvec_gb300 import metrics, mmvq, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+    type_of = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR}
+    peak, _ = load_peak()
+    cases = []
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    clocks.wait_first_sample()
+    clocks.mark()
+    for si, (fmt, rows, K) in enumerate(DECODE_SHAPES):
+        t = type_of[fmt]
+        W = torch.from_numpy(host_weights_for(fmt, rows, K, salt=si).reshape(-1)).to(dev)
+        W = mmvq.repack_planar(W, rows, K, type_=repack_source(fmt))
+        wb = metrics.weight_bytes(fmt, rows, K)
+        copies = max(2, math.ceil(2 * l2 / wb))
+        mats = [W] + [W.clone() for _ in range(copies - 1)]
+        x = torch.from_numpy(synth.activations(K, 1, salt=50 + si)).to(dev)
+        xq = torch.empty((1, K // 32, 36), dtype=torch.uint8, device=dev)
+        y = torch.empty((1, rows), device=dev)
+        n = max(copies, 20 if wb > 1e8 else 100)
+
+        def two(i):
+            mmvq.quantize_q8_1(x, out=xq)
+            mmvq.gemv(t, mats[i % copies], rows, K, xq, 1, out=y)
+
+        def one(i):
+            mmvq.gemv_f32(t, mats[i % copies], rows, K, x, 1, xq=xq, out=y)
+
+        res = {}
+        for name, fn in (("quantize_then_gemv", two), ("gemv_f32", one)):
+            for i in range(copies):
+                fn(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(device=dev)
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                for i in range(n):
+                    fn(i)
+            torch.cuda.synchronize()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            best = 1e30
+            for _ in range(5):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1) * 1e3 / n)
+            us = max_over_ranks(best, world, dev)
+            res[name] = {"us_per_step": round(us, 3), "weight_gbps": round(wb / us / 1e3, 1),
+                         "frac_of_measured": round(wb / us / 1e3 / peak, 3)}
+            del g
+        cases.append({"shape": f"{rows}x{K}", "fmt": fmt,
+                      "one_launch": mmvq.gemv_f32_fused(t, rows, K, 1), **res})
+        del mats
+        torch.cuda.empty_cache()
+    return {"workload": "one-column decode steps as a dependent chain: the quantiser and the "
+                        "product as two launches against mmvq_gemv_f32",
+            "cases": cases, "clocks": clocks.stop()}
+
+
 # --------------------------------------- the other workloads, summarised --
 
 EXTRA_WORKLOADS = ["lm_head", "q4k_dense", "q5k_dense", "moe_t1", "moe_t4", "moe_t8"]
@@ -879,6 +964,7 @@ def run_extras(args, rank, world, local_rank):
         del r
         gc.collect()
         torch.cuda.empty_cache()
+    out["decode_1col"] = run_decode(args, rank, world, local_rank)
     return out
 
 

@@ -27,6 +27,9 @@ int launch_gather_planar(const void* P, int64_t rows, int K, const int32_t* row_
 int read_device_fault(int* fault, cudaStream_t stream);
 int launch_wait_timeout_selftest(uint32_t limit_us, cudaStream_t stream);
 int dense_shape(int type, int64_t rows, int K, int ncols, int32_t* info);
+int launch_gemv_f32(int type, const void* W, int64_t rows, int K, const float* x, int64_t ldx,
+                    int ncols, void* xq, float* y, uint32_t flags, cudaStream_t s);
+int gemv_f32_fused(int type, int64_t rows, int K, int ncols, int* fused);
 int launch_route_groups(const int32_t* topk, int T, int k, int n_experts, int32_t* expert_ids,
                         int32_t* offsets, int32_t* act_index, int32_t* slot_of, int32_t* status,
                         cudaStream_t s);
@@ -134,6 +137,36 @@ int mmvq_gemv_ex(int type, const void* W, int64_t rows, int K, const void* xq, i
   if (rc) return rc;
   if (flags & ~(unsigned int)MMVQ_FLAG_XQ_STABLE) return MMVQ_ERR_SHAPE;
   return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, nullptr, flags, (cudaStream_t)stream);
+}
+
+static bool planar_type(int type) {
+  return type == MMVQ_Q4_K_PLANAR || type == MMVQ_Q5_K_PLANAR || type == MMVQ_Q6_K_PLANAR;
+}
+
+int mmvq_gemv_f32(int type, const void* W, int64_t rows, int K, const float* x, int64_t ldx,
+                  int ncols, void* xq, float* y, unsigned int flags, mmvq_stream_t stream) {
+  if (!planar_type(type)) return MMVQ_ERR_TYPE;
+  if (!W || !x || !xq || !y) return MMVQ_ERR_NULL;
+  const int rc = check_weights_shape(rows, K);
+  if (rc) return rc;
+  if (ncols < 1 || ncols > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
+  if (ldx < K) return MMVQ_ERR_SHAPE;
+  if (flags & ~(unsigned int)MMVQ_FLAG_XQ_STABLE) return MMVQ_ERR_SHAPE;
+  if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(x, 4) || !aligned(y, 4)) return MMVQ_ERR_ALIGN;
+  return mmvq::launch_gemv_f32(type, W, rows, K, x, ldx, ncols, xq, y, flags, (cudaStream_t)stream);
+}
+
+int mmvq_gemv_f32_fused(int type, int64_t rows, int K, int ncols, int32_t* fused) {
+  if (!planar_type(type)) return MMVQ_ERR_TYPE;
+  if (!fused) return MMVQ_ERR_NULL;
+  const int rc = check_weights_shape(rows, K);
+  if (rc) return rc;
+  if (ncols < 1 || ncols > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
+  int f = 0;
+  const int r2 = mmvq::gemv_f32_fused(type, rows, K, ncols, &f);
+  if (r2) return r2;
+  *fused = f;
+  return MMVQ_OK;
 }
 
 int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,

@@ -31,305 +31,9 @@
 #include <mutex>
 #include <unordered_map>
 
-#include "ring.cuh"
+#include "tma_dense.cuh"
 
 namespace mmvq {
-
-// Consumers are G groups of P warps (C = G*P); warp C is the producer.  A
-// batch is G of the row groups of the CTA's cluster (group g takes the g-th);
-// within a batch, stage bb holds, for each group, the P consecutive tiles
-// bb*P .. bb*P+P-1 of the CTA's K-range of its row group, and warp (g, p)
-// takes tile bb*P+p.  The P partial sums of a row group are added in warp
-// order at the batch end.
-//
-// K-split over a cluster (CS = 2..8 CTAs): CTA rank q of a cluster takes
-// the 256-blocks [q*nb/CS, (q+1)*nb/CS) of every row group of the cluster's
-// batches and stages only those activations, so a matrix with few row groups
-// still covers every SM, and the staged columns take 1/CS of the shared
-// memory.  At each batch end the CTAs of ranks 1..CS-1 write their row sums
-// into rank 0's shared memory (distributed shared memory) and arrive on its
-// `xfull` mbarrier (release at cluster scope); rank 0 adds them in rank order
-// after its own (a fixed order, so results repeat bit for bit) and stores y.
-// The partials are double-buffered by batch parity; before a rank overwrites
-// a buffer two batches on, it waits on its own `xempty` mbarrier, on which
-// rank 0 arrives once it has read that buffer.  Rank 0 arrives only where a
-// later batch will wait, and waits itself for every batch's partials, so no
-// CTA's shared memory is touched by another CTA after it exits.  Every wait
-// is bounded, as the ring's; a cluster barrier is passed once, after the
-// mbarriers are initialised.
-// SUMI: also store every per-32-block integer sum (the parity-debug entry);
-// a separate instance, so the product path carries no per-block test.
-// CLUSTER: the cluster instance (CS = cs); the plain instance has CS = 1
-// folded in.
-template <int LAYOUT, int NCOLS, bool SUMI, bool CLUSTER>
-__global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t* __restrict__ W,
-                                                               int64_t rows, int K,
-                                                               const uint8_t* __restrict__ xq,
-                                                               float* __restrict__ y,
-                                                               int32_t* __restrict__ sumi, int S,
-                                                               int G, int P, int cs,
-                                                               uint32_t flags) {
-  const int CS = CLUSTER ? cs : 1;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int C = G * P;  // consumer warps; warp C produces
-  const int nb = K / kQK;
-  const int nbc = nb / CS;   // 256-blocks of this CTA's K-range
-  const int Kc = K / CS;
-  const int nbq = Kc / kQK8;  // 32-blocks of the K-range (staged)
-  const int rb = act_row_bytes(Kc);
-  const int rank = CLUSTER ? (int)cluster_ctarank() : 0;
-  const int cid = blockIdx.x / CS;  // cluster index (1-D clusters of CS CTAs)
-  const int ncl = gridDim.x / CS;
-  const int64_t n_rg = (rows + kTileRows - 1) / kTileRows;
-  constexpr int TB = tile_bytes(LAYOUT);
-  const int spb = nbc / P;  // stages per batch
-  const size_t stage_bytes = (size_t)C * TB;
-
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + S;
-  volatile int* fail = reinterpret_cast<volatile int*>(empty + S);
-  uint8_t* ring = smem + tma_ring_offset(S);
-  uint8_t* act = ring + (size_t)S * stage_bytes;
-  float* da = reinterpret_cast<float*>(act + NCOLS * rb);
-  float* sa = da + NCOLS * nbq;  // Q4_K only
-  float* red = sa + (has_min(LAYOUT) ? NCOLS * nbq : 0);
-  // cluster exchange: xred [2][CS][G][NCOLS][16] floats (rank 0's is used),
-  // then xfull[2], xempty[2]
-  float* xred = red + C * kMaxCols * kTileRows;
-  uint64_t* xfull = reinterpret_cast<uint64_t*>(xred + (CS > 1 ? 2 * CS * G * NCOLS * kTileRows : 0));
-  uint64_t* xempty = xfull + 2;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C);
-    }
-    if (CLUSTER) {
-      for (int q = 0; q < 2; ++q) {
-        mbar_init(&xfull[q], (CS - 1) * G);
-        mbar_init(&xempty[q], G);
-      }
-    }
-    *fail = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  if (CLUSTER) cluster_sync_all();
-  grid_launch_dependents();
-
-  // this cluster's row groups: cid, + ncl, ... (row groups < 2^27: 32-bit
-  // divisions, which stay inline)
-  const int64_t my_rgs = (cid < n_rg) ? (uint32_t)(n_rg - 1 - cid) / ncl + 1 : 0;
-  const int64_t batches = (uint32_t)(my_rgs + G - 1) / (uint32_t)G;
-  const int64_t total = batches * spb;
-  const int64_t blk0 = (int64_t)rank * nbc;  // first 256-block of the K-range
-
-  if (warp == C) {  // ------------------------------------------ producer
-    if (lane == 0) {
-      // slot and round parity are kept incrementally (no divisions per stage)
-      int64_t it = 0;
-      int slot = 0;
-      uint32_t par = 0;
-      int64_t j = 0;
-      int bb = 0;
-      for (; it < total; ++it) {
-        if (it >= S && !*fail && !mbar_wait(&empty[slot], par ^ 1u, 128)) {
-          *fail = 1;
-          atomicOr(&g_fault_word, kFaultMbarTimeout);
-        }
-        if (*fail) break;
-        const int64_t left = my_rgs - j * G;
-        const int valid = (int)(left < G ? left : G);
-        mbar_expect_tx(&full[slot], (uint32_t)(valid * P * TB));
-        for (int g = 0; g < valid; ++g) {
-          const int64_t rg = cid + (j * G + g) * (int64_t)ncl;
-          bulk_g2s(ring + (size_t)slot * stage_bytes + (size_t)g * P * TB,
-                   W + (rg * nb + blk0 + (int64_t)bb * P) * TB, (uint32_t)(P * TB), &full[slot]);
-        }
-        if (++bb == spb) {
-          bb = 0;
-          ++j;
-        }
-        if (++slot == S) {
-          slot = 0;
-          par ^= 1u;
-        }
-      }
-      // no copy of this CTA may land after it exits: wait (bounded) for the
-      // last phase of every slot that was filled
-      const int64_t issued = it;  // a CTA's stages: < 2^31
-      for (int s = 0; s < S && s < issued; ++s) {
-        const uint32_t last = (uint32_t)(issued - 1) - ((uint32_t)(issued - 1 - s) % (uint32_t)S);
-        mbar_wait(&full[s], (last / (uint32_t)S) & 1u);
-      }
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers
-  const int nthreads = 32 * C;
-  const int tid = threadIdx.x;
-  // With MMVQ_FLAG_XQ_STABLE no kernel that may still run writes xq, so the
-  // whole product runs before the grid dependency; only the stores of y
-  // wait for the preceding kernel.
-  const bool stable = (flags & MMVQ_FLAG_XQ_STABLE) != 0;
-  bool waited = !stable;
-  if (!stable) grid_dependency_wait();
-  if constexpr (!CLUSTER) {
-    stage_q8_1(xq, K, NCOLS, [](int c) { return c; }, act, da,
-               has_min(LAYOUT) ? sa : nullptr, tid, nthreads);
-  } else {
-    stage_q8_1_slice(xq, K / kQK8, (int)blk0 * 8, Kc, NCOLS, act, da,
-                     has_min(LAYOUT) ? sa : nullptr, tid, nthreads);
-  }
-  group_sync(1, nthreads);
-
-  const int g = warp / P;
-  const int p = warp - g * P;
-  const int i = lane & 15;
-  const int h = lane >> 4;
-  int slot = 0;
-  uint32_t par = 0;
-  for (int64_t j = 0; j < batches; ++j) {
-    const int64_t k = j * G + g;
-    const bool valid = k < my_rgs;
-    const int64_t rg = cid + k * (int64_t)ncl;
-    const int64_t row = rg * kTileRows + i;
-    // per-block sums of this row at its global 32-block index
-    int32_t* srow =
-        (SUMI && sumi && valid && row < rows) ? sumi + row * (K / kQK8) + blk0 * 8 : nullptr;
-    if (srow && !waited) {
-      grid_dependency_wait();
-      waited = true;
-    }
-    float acc[NCOLS];
-#pragma unroll
-    for (int c = 0; c < NCOLS; ++c) acc[c] = 0.0f;
-    for (int bb = 0; bb < spb; ++bb) {
-      const int s = slot;
-      if (!*fail && !mbar_wait(&full[s], par)) {
-        *fail = 1;
-        atomicOr(&g_fault_word, kFaultMbarTimeout);
-      }
-      if (++slot == S) {
-        slot = 0;
-        par ^= 1u;
-      }
-      const uint8_t* tile = ring + (size_t)s * stage_bytes + (size_t)warp * TB;
-      const int64_t scs = rows * (K / kQK8);
-      if (LAYOUT == kQ4Planar) {
-        Q4Half w;
-        if (valid) load_q4_tile_smem(tile, lane, w);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q4_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
-      } else if (LAYOUT == kQ5Planar) {
-        Q5Half w;
-        if (valid) load_q5_tile_smem(tile, lane, w);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q5_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
-      } else {
-        Q6Half w;
-        if (valid) load_q6_tile_smem(tile, lane, w);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, scs);
-      }
-    }
-    // halves of each row, then the group's K-slices in warp order
-#pragma unroll
-    for (int c = 0; c < NCOLS; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
-    if (!waited) {
-      grid_dependency_wait();
-      waited = true;
-    }
-    if constexpr (!CLUSTER) {
-      if (P == 1) {
-        if (valid && h == 0 && row < rows) {
-#pragma unroll
-          for (int c = 0; c < NCOLS; ++c) y[c * rows + row] = acc[c];
-        }
-        continue;
-      }
-      if (h == 0) {
-#pragma unroll
-        for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
-      }
-      group_sync(2 + g, 32 * P);
-      if (p == 0 && valid && h == 0 && row < rows) {
-#pragma unroll
-        for (int c = 0; c < NCOLS; ++c) {
-          float sum = 0.0f;
-          for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
-          y[c * rows + row] = sum;
-        }
-      }
-      group_sync(2 + g, 32 * P);
-    } else {
-      // this CTA's sum over its P K-slices, then the cluster's K-slices:
-      // ranks 1..CS-1 send, rank 0 adds in rank order
-      float part[NCOLS];
-      if (P == 1) {
-#pragma unroll
-        for (int c = 0; c < NCOLS; ++c) part[c] = acc[c];
-      } else {
-        if (h == 0) {
-#pragma unroll
-          for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
-        }
-        group_sync(2 + g, 32 * P);
-#pragma unroll
-        for (int c = 0; c < NCOLS; ++c) {
-          float sum = 0.0f;
-          if (p == 0 && h == 0)
-            for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
-          part[c] = sum;
-        }
-      }
-      if (p == 0) {
-        const int xb = (int)(j & 1);
-        const uint32_t use = (uint32_t)(j >> 1);
-        float* slot_base = xred + (size_t)xb * CS * G * NCOLS * kTileRows;
-        if (rank != 0) {
-          if (j >= 2 && !*fail && !mbar_wait_cluster(&xempty[xb], (use - 1) & 1u)) {
-            *fail = 1;
-            atomicOr(&g_fault_word, kFaultMbarTimeout);
-          }
-          if (h == 0) {
-            float* mine = slot_base + ((size_t)(rank * G + g) * NCOLS) * kTileRows;
-#pragma unroll
-            for (int c = 0; c < NCOLS; ++c)
-              st_cluster_f32(cluster_map(mine + c * kTileRows + i, 0), part[c]);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(cluster_map(&xfull[xb], 0));
-        } else {
-          if (!*fail && !mbar_wait_cluster(&xfull[xb], use & 1u)) {
-            *fail = 1;
-            atomicOr(&g_fault_word, kFaultMbarTimeout);
-          }
-          if (valid && h == 0 && row < rows) {
-#pragma unroll
-            for (int c = 0; c < NCOLS; ++c) {
-              float sum = part[c];
-              for (int q = 1; q < CS; ++q)
-                sum += slot_base[((size_t)(q * G + g) * NCOLS + c) * kTileRows + i];
-              y[c * rows + row] = sum;
-            }
-          }
-          __syncwarp();
-          // the buffer is free again; only where a later batch waits for it
-          if (j + 2 < batches && lane > 0 && lane < CS)
-            mbar_arrive_cluster(cluster_map(&xempty[xb], lane));
-        }
-      }
-      if (P > 1) group_sync(2 + g, 32 * P);
-    }
-  }
-}
 
 // ------------------------------------------------- grouped (experts) ----
 // Grouped expert MMVQ on the same ring ("Strata" PR #2746 "B70 validation":
@@ -543,12 +247,6 @@ __global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
 
 // ------------------------------------------------------------ host side ----
 
-struct TmaCfg {
-  int G, P, slots, grid;
-  size_t smem;
-  int CS;  // CTAs per cluster (K-split); 1: no cluster
-};
-
 // Launch shape.  Candidates (G, P) with P | K/256 and C = G*P <= 12; the ring
 // gets as many stages as fit in ~110 KB (two CTAs per SM when registers
 // allow), at least two.  Cost model: a CTA's time is its batches x (stages
@@ -573,7 +271,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
       return MMVQ_OK;
     }
   }
-  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false, false>;
+  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false, false, false>;
   const int sms = device_sms();
   const size_t limit = max_smem_optin();
   if (sms <= 0 || limit == 0) return MMVQ_ERR_CUDA;
@@ -650,7 +348,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
   // 2560 x 10240 at 6 / 8 columns: 18.4 / 19.5 -> 13.1 / 14.5 us as a
   // dependent chain, 10.1 / 10.9 -> 9.9 / 11.0 us back to back.
   if (NCOLS >= 6 && nb >= 32 && (nb / 2) % 4 == 0 && best.grid < sms) {
-    auto ckern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false, true>;
+    auto ckern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, false, true, false>;
     const int G = 3, P = 4, CS = 2;
     int S = 0;
     size_t smem = 0;
@@ -708,12 +406,14 @@ static int launch_tma_cfg(const uint8_t* W, int64_t rows, int K, const uint8_t* 
                           int32_t* sumi, const TmaCfg& cfg, uint32_t flags, cudaStream_t stream) {
   if (!tma_shape_ok(cfg, K, LAYOUT, NCOLS)) return MMVQ_ERR_SHAPE;
   if (cfg.CS == 1) {
-    auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, false>;
+    auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, false, false>;
     if (ensure_smem((const void*)kern, cfg.smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
     return launch_pdl(kern, dim3(cfg.grid), dim3(32 * (cfg.G * cfg.P + 1)), cfg.smem, stream, W,
-                      rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, 1, flags);
+                      rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, 1, flags,
+                      static_cast<const float*>(nullptr), (int64_t)0,
+                      static_cast<uint8_t*>(nullptr));
   }
-  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, true>;
+  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, true, false>;
   if (ensure_smem((const void*)kern, cfg.smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(cfg.grid);
@@ -730,7 +430,8 @@ static int launch_tma_cfg(const uint8_t* W, int64_t rows, int K, const uint8_t* 
   lc.attrs = attr;
   lc.numAttrs = 2;
   return cudaLaunchKernelEx(&lc, kern, W, rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, cfg.CS,
-                            flags) == cudaSuccess
+                            flags, static_cast<const float*>(nullptr), (int64_t)0,
+                            static_cast<uint8_t*>(nullptr)) == cudaSuccess
              ? MMVQ_OK
              : MMVQ_ERR_CUDA;
 }
@@ -813,6 +514,27 @@ int launch_planar_tma_shape(int type, const void* W, int64_t rows, int K, const 
   if (layout == kQ4Planar) return launch_tma_cfg_l<kQ4Planar>(w, rows, K, x, ncols, y, sumi, c, flags, s);
   if (layout == kQ5Planar) return launch_tma_cfg_l<kQ5Planar>(w, rows, K, x, ncols, y, sumi, c, flags, s);
   return launch_tma_cfg_l<kQ6Planar>(w, rows, K, x, ncols, y, sumi, c, flags, s);
+}
+
+template <int LAYOUT>
+static int tma_config_l(int64_t rows, int K, int ncols, TmaCfg* out) {
+  switch (ncols) {
+    case 1: return tma_config<LAYOUT, 1>(rows, K, out);
+    case 2: return tma_config<LAYOUT, 2>(rows, K, out);
+    case 3: return tma_config<LAYOUT, 3>(rows, K, out);
+    case 4: return tma_config<LAYOUT, 4>(rows, K, out);
+    case 5: return tma_config<LAYOUT, 5>(rows, K, out);
+    case 6: return tma_config<LAYOUT, 6>(rows, K, out);
+    case 7: return tma_config<LAYOUT, 7>(rows, K, out);
+    case 8: return tma_config<LAYOUT, 8>(rows, K, out);
+  }
+  return MMVQ_ERR_NCOLS;
+}
+
+int planar_tma_config(int type, int64_t rows, int K, int ncols, TmaCfg* out) {
+  if (type == MMVQ_Q4_K_PLANAR) return tma_config_l<kQ4Planar>(rows, K, ncols, out);
+  if (type == MMVQ_Q5_K_PLANAR) return tma_config_l<kQ5Planar>(rows, K, ncols, out);
+  return tma_config_l<kQ6Planar>(rows, K, ncols, out);
 }
 
 template <int LAYOUT, int NCOLS>
@@ -1016,15 +738,17 @@ int launch_wait_timeout_selftest(uint32_t limit_us, cudaStream_t stream) {
 }
 
 int read_clear_ffn_fault_word(unsigned int* v);
+int read_clear_f32_fault_word(unsigned int* v);
 
 // Reads and clears the device fault words of the ring kernels and of the
 // expert layer (after synchronising `stream`); returns their OR.
 int read_device_fault(int* fault, cudaStream_t stream) {
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MMVQ_ERR_CUDA;
-  if (read_clear_fault_word(&a) != MMVQ_OK || read_clear_ffn_fault_word(&b) != MMVQ_OK)
+  if (read_clear_fault_word(&a) != MMVQ_OK || read_clear_ffn_fault_word(&b) != MMVQ_OK ||
+      read_clear_f32_fault_word(&c) != MMVQ_OK)
     return MMVQ_ERR_CUDA;
-  *fault = (int)(a | b);
+  *fault = (int)(a | b | c);
   return MMVQ_OK;
 }
 

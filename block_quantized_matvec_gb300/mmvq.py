@@ -42,6 +42,8 @@ SIGNATURES = {
     "mmvq_gemv": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P]),
     "mmvq_gemv_ex": (_I, [_I, _P, _I64, _I, _P, _I, _P, ctypes.c_uint, _P]),
     "mmvq_debug_block_sums": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P, _P]),
+    "mmvq_gemv_f32": (_I, [_I, _P, _I64, _I, _P, _I64, _I, _P, _P, ctypes.c_uint, _P]),
+    "mmvq_gemv_f32_fused": (_I, [_I, _I64, _I, _I, _P]),
     "mmvq_grouped": (_I, [_I, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P]),
     "mmvq_route_groups": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "mmvq_quantize_route_groups": (_I, [_P, _I, _I, _I64, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
@@ -149,6 +151,33 @@ def gemv(type_: int, W: torch.Tensor, rows: int, K: int, xq: torch.Tensor, ncols
         _check(lib().mmvq_gemv(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(out),
                                _stream(stream)), "mmvq_gemv")
     return out
+
+
+def gemv_f32(type_: int, W: torch.Tensor, rows: int, K: int, x: torch.Tensor, ncols: int | None = None,
+             xq: torch.Tensor | None = None, out: torch.Tensor | None = None, flags: int = 0,
+             stream=None):
+    """fp32 x [ncols, ldx] -> (y [ncols, rows], xq [ncols, K/32, 36]): Q8_1 of x and the
+    product, in one launch where the columns are small enough."""
+    _dev(W, "W")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if not x.is_cuda or x.dtype != torch.float32 or x.stride(1) != 1:
+        raise ValueError("x must be a CUDA float32 tensor with unit column stride")
+    ncols = x.shape[0] if ncols is None else ncols
+    if xq is None:
+        xq = torch.empty((ncols, K // 32, Q8_1_BYTES), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((ncols, rows), dtype=torch.float32, device=x.device)
+    _check(lib().mmvq_gemv_f32(type_, _ptr(W), rows, K, _ptr(x), x.stride(0), ncols, _ptr(xq),
+                               _ptr(out), flags, _stream(stream)), "mmvq_gemv_f32")
+    return out, xq
+
+
+def gemv_f32_fused(type_: int, rows: int, K: int, ncols: int) -> bool:
+    """Whether gemv_f32 runs this call as one launch (host-only)."""
+    f = ctypes.c_int32(0)
+    _check(lib().mmvq_gemv_f32_fused(type_, rows, K, ncols, ctypes.byref(f)), "mmvq_gemv_f32_fused")
+    return bool(f.value)
 
 
 def debug_block_sums(type_: int, W: torch.Tensor, rows: int, K: int, xq: torch.Tensor, ncols: int,

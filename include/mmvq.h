@@ -176,6 +176,28 @@ MMVQ_API int mmvq_gemv_ex(int type, const void* W, int64_t rows, int K, const vo
                           float* y, unsigned int flags, mmvq_stream_t stream);
 
 /*
+ * Dense MMVQ from fp32 activation columns: Q8_1 of x, then the product, as
+ * mmvq_quantize_q8_1 followed by mmvq_gemv_ex, with the same results (xq
+ * gets the same bytes, y the same bits).  Where the columns are small
+ * enough (a round or two of 32-blocks for the CTA's warps: one column of K
+ * up to about 5120 on the common launch shapes), it is one launch whose CTAs
+ * each quantise the columns into their own staging while their first weight
+ * stages stream in, so a decode step needs no separate quantisation launch;
+ * otherwise it issues the two launches.  x: fp32 [ncols][ldx], ldx >= K;
+ * xq: Q8_1 [ncols][K/32], written (the quantised columns); y: fp32
+ * [ncols][rows].  type: a planar type.  flags as mmvq_gemv_ex, where
+ * MMVQ_FLAG_XQ_STABLE promises that x is stable.  Other rules as mmvq_gemv.
+ * No counterpart on the pages (their engine quantises in its own launch).
+ */
+MMVQ_API int mmvq_gemv_f32(int type, const void* W, int64_t rows, int K, const float* x,
+                           int64_t ldx, int ncols, void* xq, float* y, unsigned int flags,
+                           mmvq_stream_t stream);
+
+/* Whether mmvq_gemv_f32 runs this call as one launch (*fused = 1) or as the
+ * quantiser and the product (0).  Host-only. */
+MMVQ_API int mmvq_gemv_f32_fused(int type, int64_t rows, int K, int ncols, int32_t* fused);
+
+/*
  * The per-32-block integer sums the dense product forms, for parity checks:
  * sumi: int32 [ncols][rows][K/32], sumi = sc0*sum16 + sc1*sum16 (Q6_K) or
  * sc*sum32 (Q4_K).  Runs mmvq_gemv's kernel code in the same launch shape,
