@@ -93,7 +93,8 @@ WORKLOAD_DESC = {
 
 
 MMVQ_SOURCES = ["api.cu", "common.cuh", "expert_ffn.cu", "ffn_args.cuh", "kquant.cuh", "mmvq_dense.cu",
-                "mmvq_tma.cu", "q8_1.cuh", "ring.cuh", "route.cuh", "rowgroup.cuh"]
+                "mmvq_tma.cu", "mmvq_tma_f32.cu", "q8_1.cuh", "ring.cuh", "route.cuh", "rowgroup.cuh",
+                "tma_dense.cuh"]
 
 
 def kernel_source_hash() -> str:
