@@ -17,7 +17,9 @@ times come from a second capture of the same calls with event-record nodes at
 the boundaries of each case, replayed after the timed region (an event node
 ends the programmatic chaining of the launches around it, so it stays out of
 the timed graph).  `e2e` repeats the step with the fp32 columns copied in
-from pinned host memory and all outputs read back every step.
+from pinned host memory, the calls made eagerly through the public binding
+(the C ABI, one call at a time) and all outputs read back every step;
+`e2e_graph` is the same with the calls replayed as the captured graph.
 
 The default run also times the pages' other matrices (the LM head and the
 gathered draft head at 1-5 columns, the Q4_K and Q5_K dense shapes, the MoE
@@ -324,6 +326,13 @@ def run_ours(args, rank, world, local_rank):
     y_pinned = torch.empty(y_total, dtype=torch.float32).pin_memory()
     calls_of_case = [[i for i, c in enumerate(calls) if c[0] == ci] for ci in range(len(case_list))]
 
+    # the views each call takes, made once (as a caller with preallocated
+    # buffers would)
+    x_views = [x_dev[xo:xo + nc * K].view(nc, K) for (_, _, _, K, nc, xo) in case_list]
+    y_views = [y_dev[yo:yo + case_list[ci][4] * case_list[ci][2]].view(case_list[ci][4],
+                                                                       case_list[ci][2])
+               for (ci, _, yo) in calls]
+
     def run_case(ci, s=None, evs=None, dependent=False):
         """Quantise the case's columns once, then every copy's MMVQ back to back.
         dependent=True drops the stable-activation flag: every call then waits
@@ -332,14 +341,13 @@ def run_ours(args, rank, world, local_rank):
         si, fmt, rows, K, nc, xo = case_list[ci]
         if evs is not None:
             _record_external(evs[3 * ci], s)
-        mmvq.quantize_q8_1(x_dev[xo:xo + nc * K].view(nc, K), out=xq_bufs[ci])
+        mmvq.quantize_q8_1(x_views[ci], out=xq_bufs[ci])
         if evs is not None:
             _record_external(evs[3 * ci + 1], s)
+        t = type_of[fmt]
         for n, i in enumerate(calls_of_case[ci]):
-            _, cp, yo = calls[i]
             # after the first call no kernel that may still run writes xq
-            mmvq.gemv(type_of[fmt], mats[si][cp], rows, K, xq_bufs[ci], nc,
-                      out=y_dev[yo:yo + nc * rows].view(nc, rows),
+            mmvq.gemv(t, mats[si][calls[i][1]], rows, K, xq_bufs[ci], nc, out=y_views[i],
                       flags=mmvq.FLAG_XQ_STABLE if (n and not dependent) else 0)
         if evs is not None:
             _record_external(evs[3 * ci + 2], s)
@@ -445,17 +453,29 @@ def run_ours(args, rank, world, local_rank):
     achieved = alg_step / step_s / 1e9
     achieved_instr = alg_step / (float(np.sum(g_us)) * 1e-6) / 1e9
 
-    # e2e: H2D of the step's columns, the step, D2H of every output, each step
-    # (left out for the extra workloads of the default run)
-    e2e_steps = 0 if getattr(args, "light", False) else max(3, min(args.steps, 200))
-    torch.cuda.synchronize()
-    w0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        x_dev.copy_(x_pinned, non_blocking=True)
-        graph.replay()
-        y_pinned.copy_(y_dev, non_blocking=True)
+    # e2e: every step, H2D of the step's fp32 columns from pinned memory, the
+    # step's calls made eagerly through the public binding (each a ctypes call
+    # into the C ABI: argument checks, launch), D2H of every output, a
+    # synchronise; the same with the calls replayed as the captured graph is
+    # reported beside it (e2e_graph).  Left out for the extra workloads.
+    e2e_steps = 0 if getattr(args, "light", False) else max(3, min(args.steps // 3, 100))
+
+    def e2e_time(replay):
         torch.cuda.synchronize()
-    e2e_s = max_over_ranks((time.perf_counter() - w0) / max(1, e2e_steps), world, dev)
+        w0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            x_dev.copy_(x_pinned, non_blocking=True)
+            if replay:
+                graph.replay()
+            else:
+                for ci in range(len(case_list)):
+                    run_case(ci)
+            y_pinned.copy_(y_dev, non_blocking=True)
+            torch.cuda.synchronize()
+        return max_over_ranks((time.perf_counter() - w0) / max(1, e2e_steps), world, dev)
+
+    e2e_s = e2e_time(False) if e2e_steps else 1.0
+    e2e_graph_s = e2e_time(True) if e2e_steps else 1.0
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -485,7 +505,13 @@ def run_ours(args, rank, world, local_rank):
                      "achieved_instrumented": round(achieved_instr, 1)},
         "e2e": ({"value": round(world * w_step / e2e_s / 1e9, 1), "unit": UNIT,
                  "h2d_bytes_per_step": int(x_host.nbytes), "d2h_bytes_per_step": int(y_total * 4),
-                 "steps": e2e_steps} if e2e_steps else None),
+                 "steps": e2e_steps, "ms_per_step": round(e2e_s * 1e3, 3),
+                 "calls": "eager: mmvq.quantize_q8_1 + mmvq.gemv per case through the C ABI"}
+                if e2e_steps else None),
+        "e2e_graph": ({"value": round(world * w_step / e2e_graph_s / 1e9, 1), "unit": UNIT,
+                       "ms_per_step": round(e2e_graph_s * 1e3, 3),
+                       "calls": "the same calls replayed as the captured CUDA graph"}
+                      if e2e_steps else None),
         "gpu_launches": (len(calls) + len(case_list)) * args.steps,
         "clocks": clk,
         "cases": per_case,

@@ -78,6 +78,8 @@ _lib = None
 def lib() -> ctypes.CDLL:
     """The loaded C-ABI library.  Raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -106,9 +108,17 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+# The current stream's handle without building a torch Stream object (about
+# 3 us a call otherwise); torch's own raw accessor where it exists.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dev(t: torch.Tensor, name: str):
