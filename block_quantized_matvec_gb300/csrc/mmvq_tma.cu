@@ -282,12 +282,20 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
   double best_cost = 1e300;
   int best_c = 0;
   // Very tall matrices (an LM head): one warp per row group (no K-split, no
-  // barriers), seven row groups per CTA, a two-stage ring, so that three
-  // CTAs (21 consumer warps) share each SM.  Measured on GB300: ~15% faster
-  // than the split-K shapes for 151936 x 2560.
+  // barriers), a two-stage ring, several CTAs per SM.  Measured on GB300:
+  // ~15% faster than the split-K shapes for 151936 x 2560.
+  // At one column, four CTAs of four row groups per SM: a persistent CTA
+  // takes a fixed share of the row groups, and CTAs finish up to ~17 us
+  // apart in a 50 us head call (measured per CTA); with more, smaller
+  // CTAs per SM the spread shrinks.  Measured for 151936 x 2560 at one
+  // column: 44.8 / 47.0 us back to back / dependent, against 44.0 / 51.2 us
+  // for seven row groups, three CTAs per SM, which stays best from two
+  // columns on (a fourth CTA of seven row groups was ~6% slower there).
   const bool tall = n_rg >= (int64_t)16 * sms;
   if (tall) {
-    for (int G = 7; G >= 1 && best.G == 0; --G) {
+    const int g_top = NCOLS == 1 ? 4 : 7;
+    const int per_cap = NCOLS == 1 ? 4 : 3;
+    for (int G = g_top; G >= 1 && best.G == 0; --G) {
       const size_t smem = tma_smem_bytes(LAYOUT, 2, K, NCOLS, G, 1);
       if (smem > limit) continue;
       if (ensure_smem((const void*)kern, smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
@@ -296,9 +304,7 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
           cudaSuccess)
         return MMVQ_ERR_CUDA;
       if (per_sm < 1) continue;
-      // at most three resident CTAs per SM, as measured (a fourth, where
-      // registers allow it, made the one-column head ~6% slower)
-      per_sm = std::min(per_sm, 3);
+      per_sm = std::min(per_sm, per_cap);
       const int64_t ctas = std::min<int64_t>((n_rg + G - 1) / G, (int64_t)sms * per_sm);
       best = {G, 1, 2, (int)ctas, smem, 1};
     }
