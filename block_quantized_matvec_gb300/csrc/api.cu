@@ -135,7 +135,7 @@ int mmvq_gemv_ex(int type, const void* W, int64_t rows, int K, const void* xq, i
                  unsigned int flags, mmvq_stream_t stream) {
   const int rc = gemv_checks(type, W, rows, K, xq, ncols, y);
   if (rc) return rc;
-  if (flags & ~(unsigned int)MMVQ_FLAG_XQ_STABLE) return MMVQ_ERR_SHAPE;
+  if (flags & ~(unsigned int)(MMVQ_FLAG_XQ_STABLE | MMVQ_FLAG_TENSOR_CORE)) return MMVQ_ERR_SHAPE;
   return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, nullptr, flags, (cudaStream_t)stream);
 }
 
@@ -151,7 +151,7 @@ int mmvq_gemv_f32(int type, const void* W, int64_t rows, int K, const float* x, 
   if (rc) return rc;
   if (ncols < 1 || ncols > mmvq::kMaxCols) return MMVQ_ERR_NCOLS;
   if (ldx < K) return MMVQ_ERR_SHAPE;
-  if (flags & ~(unsigned int)MMVQ_FLAG_XQ_STABLE) return MMVQ_ERR_SHAPE;
+  if (flags & ~(unsigned int)(MMVQ_FLAG_XQ_STABLE | MMVQ_FLAG_TENSOR_CORE)) return MMVQ_ERR_SHAPE;
   if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(x, 4) || !aligned(y, 4)) return MMVQ_ERR_ALIGN;
   return mmvq::launch_gemv_f32(type, W, rows, K, x, ldx, ncols, xq, y, flags, (cudaStream_t)stream);
 }
@@ -171,11 +171,18 @@ int mmvq_gemv_f32_fused(int type, int64_t rows, int K, int ncols, int32_t* fused
 
 int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
                           int32_t* sumi, float* y, mmvq_stream_t stream) {
+  return mmvq_debug_block_sums_ex(type, W, rows, K, xq, ncols, sumi, y, 0u, stream);
+}
+
+int mmvq_debug_block_sums_ex(int type, const void* W, int64_t rows, int K, const void* xq,
+                             int ncols, int32_t* sumi, float* y, unsigned int flags,
+                             mmvq_stream_t stream) {
   const int rc = gemv_checks(type, W, rows, K, xq, ncols, sumi);
   if (rc) return rc;
   if (!y) return MMVQ_ERR_NULL;
   if (!aligned(y, 4)) return MMVQ_ERR_ALIGN;
-  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, sumi, 0u, (cudaStream_t)stream);
+  if (flags & ~(unsigned int)(MMVQ_FLAG_XQ_STABLE | MMVQ_FLAG_TENSOR_CORE)) return MMVQ_ERR_SHAPE;
+  return mmvq::launch_dense(type, W, rows, K, xq, ncols, y, sumi, flags, (cudaStream_t)stream);
 }
 
 int mmvq_grouped(int type, const void* W_experts, int n_experts, int64_t rows, int K,

@@ -27,8 +27,13 @@ constexpr int kMaxK = 16384;
 
 // Activation quants in shared memory: per column, K bytes with 16 bytes of
 // padding after every 128 (four Q8_1 blocks), so that the two halves of a
-// 256-block (lanes 0-15 and 16-31 of a warp) hit different banks.
-__host__ __device__ constexpr int act_row_bytes(int K) { return K + K / 8; }
+// 256-block (lanes 0-15 and 16-31 of a warp) hit different banks, and the
+// column stride rounded up to 16 more than a multiple of 128 bytes, so that
+// eight lanes reading the same word of eight columns hit eight different
+// groups of four banks (the tensor-core consumer's activation fragments).
+__host__ __device__ constexpr int act_row_bytes(int K) {
+  return K + K / 8 + (((16 - (K + K / 8)) % 128) + 128) % 128;
+}
 __device__ __forceinline__ int act_off(int kb) { return kb * 32 + (kb >> 2) * 16; }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {

@@ -396,30 +396,31 @@ static int tma_config(int64_t rows, int K, TmaCfg* out) {
 // A launch shape the kernel can run: a ring of at least two stages, at most
 // 12 consumer warps, CS | K/256 and P | (K/256)/CS, a grid of whole clusters
 // of 1-8 CTAs, and the shared memory the shape needs.
-static bool tma_shape_ok(const TmaCfg& c, int K, int layout, int ncols) {
+static bool tma_shape_ok(const TmaCfg& c, int K, int layout, int ncols, bool mma) {
   const int nb = K / kQK;
   if (c.slots < 2 || c.G < 1 || c.P < 1 || c.G * c.P > 12) return false;
   if (c.CS < 1 || c.CS > 8) return false;
   if (nb % c.CS != 0 || (nb / c.CS) % c.P != 0 || c.grid < c.CS || c.grid % c.CS != 0) return false;
-  return c.smem >= tma_smem_bytes(layout, c.slots, K, ncols, c.G, c.P, c.CS) &&
+  return c.smem >= tma_smem_bytes(layout, c.slots, K, ncols, c.G, c.P, c.CS, mma) &&
          c.smem <= max_smem_optin();
 }
 
 // The instance that also stores the per-block sums runs in the product
 // instance's launch shape, so y comes out with the same bits.
-template <int LAYOUT, int NCOLS, bool SUMI>
-static int launch_tma_cfg(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
-                          int32_t* sumi, const TmaCfg& cfg, uint32_t flags, cudaStream_t stream) {
-  if (!tma_shape_ok(cfg, K, LAYOUT, NCOLS)) return MMVQ_ERR_SHAPE;
+template <int LAYOUT, int NCOLS, bool SUMI, bool MMA>
+static int launch_tma_cfg_k(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
+                            int32_t* sumi, const TmaCfg& cfg, uint32_t flags,
+                            cudaStream_t stream) {
+  if (!tma_shape_ok(cfg, K, LAYOUT, NCOLS, MMA)) return MMVQ_ERR_SHAPE;
   if (cfg.CS == 1) {
-    auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, false, false>;
+    auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, false, false, MMA>;
     if (ensure_smem((const void*)kern, cfg.smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
     return launch_pdl(kern, dim3(cfg.grid), dim3(32 * (cfg.G * cfg.P + 1)), cfg.smem, stream, W,
                       rows, K, xq, y, sumi, cfg.slots, cfg.G, cfg.P, 1, flags,
                       static_cast<const float*>(nullptr), (int64_t)0,
                       static_cast<uint8_t*>(nullptr));
   }
-  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, true, false>;
+  auto kern = mmvq_planar_tma_kernel<LAYOUT, NCOLS, SUMI, true, false, MMA>;
   if (ensure_smem((const void*)kern, cfg.smem) != MMVQ_OK) return MMVQ_ERR_CUDA;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(cfg.grid);
@@ -440,6 +441,31 @@ static int launch_tma_cfg(const uint8_t* W, int64_t rows, int K, const uint8_t* 
                             static_cast<uint8_t*>(nullptr)) == cudaSuccess
              ? MMVQ_OK
              : MMVQ_ERR_CUDA;
+}
+
+// The consumer of the shape (cfg.mma, set by the explicit-shape entry), or
+// with MMVQ_FLAG_TENSOR_CORE the tensor-core one in the chosen shape, its
+// table added to the shared memory where that still fits (the dp4a
+// consumer otherwise: same sums, same bits).
+template <int LAYOUT, int NCOLS, bool SUMI>
+static int launch_tma_cfg(const uint8_t* W, int64_t rows, int K, const uint8_t* xq, float* y,
+                          int32_t* sumi, const TmaCfg& cfg, uint32_t flags, cudaStream_t stream) {
+  if constexpr (NCOLS >= kMmaMinCols) {
+    if (cfg.mma)
+      return launch_tma_cfg_k<LAYOUT, NCOLS, SUMI, true>(W, rows, K, xq, y, sumi, cfg, flags,
+                                                         stream);
+    if (flags & MMVQ_FLAG_TENSOR_CORE) {
+      TmaCfg m = cfg;
+      m.smem = tma_smem_bytes(LAYOUT, cfg.slots, K, NCOLS, cfg.G, cfg.P, cfg.CS, true);
+      m.mma = 1;
+      if (m.smem <= max_smem_optin())
+        return launch_tma_cfg_k<LAYOUT, NCOLS, SUMI, true>(W, rows, K, xq, y, sumi, m, flags,
+                                                           stream);
+    }
+  } else {
+    if (cfg.mma) return MMVQ_ERR_SHAPE;
+  }
+  return launch_tma_cfg_k<LAYOUT, NCOLS, SUMI, false>(W, rows, K, xq, y, sumi, cfg, flags, stream);
 }
 
 template <int LAYOUT, int NCOLS, bool SUMI>
@@ -510,11 +536,13 @@ static int launch_tma_cfg_l(const uint8_t* w, int64_t rows, int K, const uint8_t
 // the shared memory the shape needs; the shape is checked as the chooser's.
 int launch_planar_tma_shape(int type, const void* W, int64_t rows, int K, const void* xq,
                             int ncols, float* y, int32_t* sumi, int G, int P, int S, int CS,
-                            int grid, uint32_t flags, cudaStream_t s) {
+                            int grid, int mma, uint32_t flags, cudaStream_t s) {
   const int layout =
       type == MMVQ_Q4_K_PLANAR ? kQ4Planar : type == MMVQ_Q5_K_PLANAR ? kQ5Planar : kQ6Planar;
   if (G < 1 || P < 1 || S < 2 || CS < 1 || CS > 8) return MMVQ_ERR_SHAPE;
-  TmaCfg c = {G, P, S, grid, tma_smem_bytes(layout, S, K, ncols, G, P, CS), CS};
+  if (mma && ncols < kMmaMinCols) return MMVQ_ERR_SHAPE;
+  TmaCfg c = {G, P, S, grid, tma_smem_bytes(layout, S, K, ncols, G, P, CS, mma != 0), CS,
+              mma ? 1 : 0};
   const uint8_t* w = static_cast<const uint8_t*>(W);
   const uint8_t* x = static_cast<const uint8_t*>(xq);
   if (layout == kQ4Planar) return launch_tma_cfg_l<kQ4Planar>(w, rows, K, x, ncols, y, sumi, c, flags, s);

@@ -58,9 +58,12 @@ static int launch_f32_l(const uint8_t* W, int64_t rows, int K, const float* x, i
 // LM head, three CTAs per SM) would quantise the columns in hundreds of CTAs
 // for a product of tens of microseconds (measured 53.5 against 50.1 us per
 // head step as two launches).
-static bool f32_fuses(const TmaCfg& cfg, int ncols, int K) {
+// MMVQ_FLAG_TENSOR_CORE: the fp32 instance is a dp4a one, so the flag
+// takes the two launches.
+static bool f32_fuses(const TmaCfg& cfg, int ncols, int K, uint32_t flags) {
   const int nquads = 8 * cfg.G * cfg.P;  // consumer threads / 4
-  return cfg.CS == 1 && ncols * (K / kQK8) <= kF32MaxRounds * nquads &&
+  return cfg.CS == 1 && !(flags & MMVQ_FLAG_TENSOR_CORE) &&
+         ncols * (K / kQK8) <= kF32MaxRounds * nquads &&
          cfg.grid <= 2 * device_sms();
 }
 
@@ -70,7 +73,7 @@ int gemv_f32_fused(int type, int64_t rows, int K, int ncols, int* fused) {
   TmaCfg cfg;
   const int rc = planar_tma_config(type, rows, K, ncols, &cfg);
   if (rc != MMVQ_OK) return rc;
-  *fused = f32_fuses(cfg, ncols, K) ? 1 : 0;
+  *fused = f32_fuses(cfg, ncols, K, 0u) ? 1 : 0;
   return MMVQ_OK;
 }
 
@@ -80,7 +83,7 @@ int launch_gemv_f32(int type, const void* W, int64_t rows, int K, const float* x
   int rc = planar_tma_config(type, rows, K, ncols, &cfg);
   if (rc != MMVQ_OK) return rc;
   uint8_t* q = static_cast<uint8_t*>(xq);
-  if (!f32_fuses(cfg, ncols, K)) {
+  if (!f32_fuses(cfg, ncols, K, flags)) {
     rc = launch_quantize_q8_1(x, K, ncols, ldx, xq, s);
     if (rc != MMVQ_OK) return rc;
     return launch_planar_tma(type, W, rows, K, xq, ncols, y, nullptr, flags, s);

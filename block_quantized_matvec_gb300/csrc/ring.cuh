@@ -173,13 +173,16 @@ __host__ __device__ constexpr int tile_bytes(int layout) {
 }
 // With a K-split over a cluster of CS CTAs each stages K/CS of the
 // activations and holds the exchange buffers [2][CS][G][ncols][16] floats
-// and two pairs of mbarriers.
+// and two pairs of mbarriers.  mma: the tensor-core consumer's table of
+// 32 floats per 32-block (tma_mma.cuh).
 __host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int ncols, int G, int P,
-                                                 int CS = 1) {
+                                                 int CS = 1, bool mma = false) {
   const int C = G * P;
   const int Kc = K / CS;
-  return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + (size_t)ncols * act_row_bytes(Kc) +
-         (size_t)ncols * (Kc / kQK8) * 4 * (has_min(layout) ? 2 : 1) +
+  const size_t cols = (size_t)ncols * act_row_bytes(Kc) +
+                      (size_t)ncols * (Kc / kQK8) * 4 * (has_min(layout) ? 2 : 1) +
+                      (mma ? (size_t)(Kc / kQK8) * 32 * 4 : 0);
+  return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + cols +
          (size_t)C * kMaxCols * kTileRows * 4 +
          (CS > 1 ? (size_t)2 * CS * G * ncols * kTileRows * 4 + 32 : 0);
 }

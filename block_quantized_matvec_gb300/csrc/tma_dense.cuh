@@ -5,7 +5,7 @@
 // notes are at the top of mmvq_tma.cu.
 #pragma once
 #include "q8_1.cuh"
-#include "ring.cuh"
+#include "tma_mma.cuh"
 
 namespace mmvq {
 
@@ -87,7 +87,13 @@ __device__ __forceinline__ void quantize_columns_quad(const float* __restrict__ 
 // XF32: the columns come as fp32 x [NCOLS][ldx] and the CTA quantises them
 // itself into its staging (a 32-block per four lanes, the plain quantiser's
 // bytes); CTA 0 also writes them to xq (plain instance only).
-template <int LAYOUT, int NCOLS, bool SUMI, bool CLUSTER, bool XF32>
+// MMA: the tensor-core consumer (tma_mma.cuh; same sums, same bits) on the
+// same staging, plus a table of d_a, s_a and MMA start values built after
+// it; MMA lane (g, t) holds rows g and g + 8, columns 2t and 2t + 1, and
+// both halves of each block, and the lane sums pass through shared memory
+// into the dp4a lanes' layout before the K-slice reduction, which is
+// common to both.
+template <int LAYOUT, int NCOLS, bool SUMI, bool CLUSTER, bool XF32, bool MMA = false>
 __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t* __restrict__ W,
                                                                int64_t rows, int K,
                                                                const uint8_t* __restrict__ xq,
@@ -97,7 +103,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
                                                                uint32_t flags,
                                                                const float* __restrict__ xf,
                                                                int64_t ldx, uint8_t* xq_out) {
-  static_assert(!(XF32 && (CLUSTER || SUMI)), "fp32 columns: plain product instance only");
+  static_assert(!(XF32 && (CLUSTER || SUMI || MMA)), "fp32 columns: plain dp4a instance only");
   const int CS = CLUSTER ? cs : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
@@ -123,7 +129,8 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   uint8_t* act = ring + (size_t)S * stage_bytes;
   float* da = reinterpret_cast<float*>(act + NCOLS * rb);
   float* sa = da + NCOLS * nbq;  // Q4_K only
-  float* red = sa + (has_min(LAYOUT) ? NCOLS * nbq : 0);
+  float* tab = sa + (has_min(LAYOUT) ? NCOLS * nbq : 0);  // MMA: [nbq][4][8]
+  float* red = tab + (MMA ? nbq * 32 : 0);
   // cluster exchange: xred [2][CS][G][NCOLS][16] floats (rank 0's is used),
   // then xfull[2], xempty[2]
   float* xred = red + C * kMaxCols * kTileRows;
@@ -217,11 +224,17 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
                      has_min(LAYOUT) ? sa : nullptr, tid, nthreads);
   }
   group_sync(1, nthreads);
+  if constexpr (MMA) {
+    mma_build_table<LAYOUT>(act, rb, da, sa, nbq, NCOLS, tab, tid, nthreads);
+    group_sync(1, nthreads);
+  }
 
   const int g = warp / P;
   const int p = warp - g * P;
   const int i = lane & 15;
   const int h = lane >> 4;
+  const int mg = lane >> 2;  // MMA lane (mg, mt): rows mg, mg + 8; columns 2mt, 2mt + 1
+  const int mt = lane & 3;
   int slot = 0;
   uint32_t par = 0;
   for (int64_t j = 0; j < batches; ++j) {
@@ -239,6 +252,19 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
     float acc[NCOLS];
 #pragma unroll
     for (int c = 0; c < NCOLS; ++c) acc[c] = 0.0f;
+    float macc[2][2][2] = {{{0.0f, 0.0f}, {0.0f, 0.0f}}, {{0.0f, 0.0f}, {0.0f, 0.0f}}};
+    int32_t* msrow[2] = {nullptr, nullptr};
+    if (SUMI && MMA && sumi && valid) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int64_t mrow = rg * kTileRows + mg + 8 * rr;
+        if (mrow < rows) msrow[rr] = sumi + mrow * (K / kQK8) + blk0 * 8;
+      }
+      if ((msrow[0] || msrow[1]) && !waited) {
+        grid_dependency_wait();
+        waited = true;
+      }
+    }
     for (int bb = 0; bb < spb; ++bb) {
       const int s = slot;
       if (!*fail && !mbar_wait(&full[s], par)) {
@@ -251,7 +277,23 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
       }
       const uint8_t* tile = ring + (size_t)s * stage_bytes + (size_t)warp * TB;
       const int64_t scs = rows * (K / kQK8);
-      if (LAYOUT == kQ4Planar) {
+      if constexpr (MMA) {
+        if (LAYOUT == kQ6Planar) {
+          Q6Mma w;
+          if (valid) load_q6_mma(tile, mg, mt, w);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          if (valid) q6_mma<NCOLS, SUMI>(w, bb * P + p, lane, act, rb, tab, macc, msrow, scs);
+        } else {
+          Q45Mma w;
+          if (valid) load_q45_mma<LAYOUT == kQ5Planar>(tile, mg, mt, w);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          if (valid)
+            q45_mma<NCOLS, LAYOUT == kQ5Planar, SUMI>(w, bb * P + p, lane, act, rb, tab, macc,
+                                                      msrow, scs);
+        }
+      } else if (LAYOUT == kQ4Planar) {
         Q4Half w;
         if (valid) load_q4_tile_smem(tile, lane, w);
         __syncwarp();
@@ -272,8 +314,26 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
       }
     }
     // halves of each row, then the group's K-slices in warp order
+    if constexpr (MMA) {
+      // the MMA lanes' row sums into the dp4a lanes' layout (row i, all
+      // columns on lanes i and 16 + i), through this warp's partials
+      float* wred = red + (size_t)warp * kMaxCols * kTileRows;
+      __syncwarp();
 #pragma unroll
-    for (int c = 0; c < NCOLS; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col = 2 * mt + cc;
+          if (col < NCOLS) wred[col * kTileRows + mg + 8 * rr] = macc[rr][cc][0] + macc[rr][cc][1];
+        }
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < NCOLS; ++c) acc[c] = wred[c * kTileRows + i];
+      __syncwarp();
+    } else {
+#pragma unroll
+      for (int c = 0; c < NCOLS; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
+    }
     if (!waited) {
       grid_dependency_wait();
       waited = true;
@@ -368,8 +428,12 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
 struct TmaCfg {
   int G, P, slots, grid;
   size_t smem;
-  int CS;  // CTAs per cluster (K-split); 1: no cluster
+  int CS;       // CTAs per cluster (K-split); 1: no cluster
+  int mma = 0;  // 1: the tensor-core consumer (tma_mma.cuh)
 };
+
+// Column counts with a tensor-core instance (MMVQ_FLAG_TENSOR_CORE).
+constexpr int kMmaMinCols = 4;
 
 // The launch shape mmvq_gemv takes for a planar matrix (mmvq_tma.cu).
 int planar_tma_config(int type, int64_t rows, int K, int ncols, TmaCfg* out);

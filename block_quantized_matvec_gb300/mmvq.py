@@ -29,6 +29,7 @@ MAX_COLS = 8
 
 OK = 0
 FLAG_XQ_STABLE = 1
+FLAG_TENSOR_CORE = 2
 ERR_TYPE, ERR_SHAPE, ERR_NCOLS, ERR_NULL, ERR_ALIGN, ERR_ROUTING, ERR_CUDA = -1, -2, -3, -4, -5, -6, -7
 ERR_SCRATCH = -8
 NOALLOC_SCRATCH_BYTES = 2 << 20  # MMVQ_NOALLOC_SCRATCH_BYTES
@@ -42,6 +43,7 @@ SIGNATURES = {
     "mmvq_gemv": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P]),
     "mmvq_gemv_ex": (_I, [_I, _P, _I64, _I, _P, _I, _P, ctypes.c_uint, _P]),
     "mmvq_debug_block_sums": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P, _P]),
+    "mmvq_debug_block_sums_ex": (_I, [_I, _P, _I64, _I, _P, _I, _P, _P, ctypes.c_uint, _P]),
     "mmvq_gemv_f32": (_I, [_I, _P, _I64, _I, _P, _I64, _I, _P, _P, ctypes.c_uint, _P]),
     "mmvq_gemv_f32_fused": (_I, [_I, _I64, _I, _I, _P]),
     "mmvq_grouped": (_I, [_I, _P, _I, _I64, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P]),
@@ -149,7 +151,8 @@ def quantize_q8_1(x: torch.Tensor, K: int | None = None, out: torch.Tensor | Non
 def gemv(type_: int, W: torch.Tensor, rows: int, K: int, xq: torch.Tensor, ncols: int,
          out: torch.Tensor | None = None, stream=None, flags: int = 0) -> torch.Tensor:
     """y [ncols, rows] fp32 = W (rows x K, block type ``type_``) times ncols Q8_1 columns.
-    flags: FLAG_XQ_STABLE when no still-running kernel writes xq (mmvq_gemv_ex)."""
+    flags: FLAG_XQ_STABLE when no still-running kernel writes xq, FLAG_TENSOR_CORE for
+    the tensor-core consumer (mmvq_gemv_ex)."""
     _dev(W, "W")
     _dev(xq, "xq")
     if out is None:
@@ -191,14 +194,19 @@ def gemv_f32_fused(type_: int, rows: int, K: int, ncols: int) -> bool:
 
 
 def debug_block_sums(type_: int, W: torch.Tensor, rows: int, K: int, xq: torch.Tensor, ncols: int,
-                     stream=None):
+                     stream=None, flags: int = 0):
     """(sumi [ncols, rows, K/32] int32, y [ncols, rows]) from the gemv kernel itself."""
     _dev(W, "W")
     _dev(xq, "xq")
     sumi = torch.empty((ncols, rows, K // 32), dtype=torch.int32, device=W.device)
     y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
-    _check(lib().mmvq_debug_block_sums(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(sumi),
-                                       _ptr(y), _stream(stream)), "mmvq_debug_block_sums")
+    if flags:
+        _check(lib().mmvq_debug_block_sums_ex(type_, _ptr(W), rows, K, _ptr(xq), ncols,
+                                              _ptr(sumi), _ptr(y), flags, _stream(stream)),
+               "mmvq_debug_block_sums_ex")
+    else:
+        _check(lib().mmvq_debug_block_sums(type_, _ptr(W), rows, K, _ptr(xq), ncols, _ptr(sumi),
+                                           _ptr(y), _stream(stream)), "mmvq_debug_block_sums")
     return sumi, y
 
 

@@ -108,7 +108,15 @@ enum mmvq_flags {
    * since writes it; those quantisers never let their successor start
    * early).  The product then runs before waiting for the preceding kernel,
    * and only the stores of y wait for it. */
-  MMVQ_FLAG_XQ_STABLE = 1
+  MMVQ_FLAG_XQ_STABLE = 1,
+  /* Planar types, 4-8 columns: form the integer sums with warp-level f16
+   * tensor-core MMAs (one per 16-weight sub-block, exact) instead of dp4a,
+   * in the same launch shape; the per-block sums and y are the same, bit
+   * for bit.  Measured on GB300 it is no faster than dp4a at 8 columns and
+   * slower below, so the default stays dp4a (the calls are latency-bound,
+   * not bound by the dp4a issue rate).  Ignored where the extra 4 bytes of
+   * shared memory per value of K do not fit, and by the GGUF types. */
+  MMVQ_FLAG_TENSOR_CORE = 2
 };
 
 enum mmvq_status {
@@ -207,6 +215,12 @@ MMVQ_API int mmvq_gemv_f32_fused(int type, int64_t rows, int K, int ncols, int32
  */
 MMVQ_API int mmvq_debug_block_sums(int type, const void* W, int64_t rows, int K, const void* xq, int ncols,
                           int32_t* sumi, float* y, mmvq_stream_t stream);
+
+/* mmvq_debug_block_sums with the flags of mmvq_gemv_ex (MMVQ_FLAG_TENSOR_CORE:
+ * the sums as the tensor-core consumer forms them). */
+MMVQ_API int mmvq_debug_block_sums_ex(int type, const void* W, int64_t rows, int K,
+                                      const void* xq, int ncols, int32_t* sumi, float* y,
+                                      unsigned int flags, mmvq_stream_t stream);
 
 /*
  * Grouped expert MMVQ over per-expert token lists (PR #2746 "B70

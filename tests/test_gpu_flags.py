@@ -49,4 +49,4 @@ def test_flagged_chain_sees_each_new_activation():
 def test_unknown_flag_bits_are_rejected():
     t = torch.zeros(4096, dtype=torch.uint8, device="cuda")
     with pytest.raises(mmvq.MMVQError):
-        mmvq.gemv(mmvq.TYPE_Q6_K_PLANAR, t, 16, 256, t, 1, out=torch.empty(16, device="cuda"), flags=2)
+        mmvq.gemv(mmvq.TYPE_Q6_K_PLANAR, t, 16, 256, t, 1, out=torch.empty(16, device="cuda"), flags=4)
