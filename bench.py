@@ -96,7 +96,7 @@ WORKLOAD_DESC = {
 
 MMVQ_SOURCES = ["api.cu", "common.cuh", "expert_ffn.cu", "ffn_args.cuh", "kquant.cuh", "mmvq_dense.cu",
                 "mmvq_tma.cu", "mmvq_tma_f32.cu", "q8_1.cuh", "ring.cuh", "route.cuh", "rowgroup.cuh",
-                "tma_dense.cuh"]
+                "tma_dense.cuh", "tma_mma.cuh"]
 
 
 def kernel_source_hash() -> str:
@@ -953,6 +953,81 @@ def run_decode(args, rank, world, local_rank):
             "cases": cases, "clocks": clocks.stop()}
 
 
+TENSOR_CORE_SHAPES = [("q6_k_planar", 2560, 2560), ("q6_k_planar", 2560, 10240),
+                      ("q6_k_planar", 10240, 2560), ("q4_k_planar", 12288, 2560)]
+
+
+def run_tensor_core(args, rank, world, local_rank):
+    """The tensor-core consumer (MMVQ_FLAG_TENSOR_CORE) against the default
+    dp4a consumer in the same launch shape, at 4, 6 and 8 columns: calls
+    back to back (each after the first with MMVQ_FLAG_XQ_STABLE) over
+    rotating weight copies > 2x L2, as CUDA graphs; us per call for each and
+    whether y has the same bits."""
+    import torch
+    from block_quantized_matvec_gb300 import metrics, mmvq, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+    type_of = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q4_k_planar": mmvq.TYPE_Q4_K_PLANAR}
+    cases = []
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    clocks.wait_first_sample()
+    clocks.mark()
+    for si, (fmt, rows, K) in enumerate(TENSOR_CORE_SHAPES):
+        t = type_of[fmt]
+        W = torch.from_numpy(host_weights_for(fmt, rows, K, salt=si).reshape(-1)).to(dev)
+        W = mmvq.repack_planar(W, rows, K, type_=repack_source(fmt))
+        wb = metrics.weight_bytes(fmt, rows, K)
+        copies = max(2, math.ceil(2 * l2 / wb))
+        mats = [W] + [W.clone() for _ in range(copies - 1)]
+        n = max(copies, 100)
+        for nc in (4, 6, 8):
+            xq = mmvq.quantize_q8_1(torch.from_numpy(synth.activations(K, nc, salt=70 + si)).to(dev))
+            y = torch.empty((nc, rows), device=dev)
+            res = {}
+            for name, base in (("dp4a", 0), ("tensor_core", mmvq.FLAG_TENSOR_CORE)):
+                def fn(i, base=base):
+                    mmvq.gemv(t, mats[i % copies], rows, K, xq, nc, out=y,
+                              flags=base | (mmvq.FLAG_XQ_STABLE if i else 0))
+                for i in range(copies):
+                    fn(i)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream(device=dev)
+                cap.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                    for i in range(n):
+                        fn(i)
+                torch.cuda.synchronize()
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                best = 1e30
+                for _ in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    g.replay()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    best = min(best, e0.elapsed_time(e1) * 1e3 / n)
+                res[name] = round(max_over_ranks(best, world, dev), 3)
+                del g
+            y0 = mmvq.gemv(t, mats[0], rows, K, xq, nc)
+            y1 = mmvq.gemv(t, mats[0], rows, K, xq, nc, flags=mmvq.FLAG_TENSOR_CORE)
+            cases.append({"shape": f"{rows}x{K}", "fmt": fmt, "ncols": nc,
+                          "us_per_call_dp4a": res["dp4a"],
+                          "us_per_call_tensor_core": res["tensor_core"],
+                          "same_bits": bool(torch.equal(y0.view(torch.int32), y1.view(torch.int32)))})
+        del mats
+        torch.cuda.empty_cache()
+    return {"workload": "4-8 columns, the tensor-core consumer (MMVQ_FLAG_TENSOR_CORE) against the "
+                        "dp4a consumer in the same launch shape, calls back to back",
+            "cases": cases, "clocks": clocks.stop()}
+
+
 # --------------------------------------- the other workloads, summarised --
 
 EXTRA_WORKLOADS = ["lm_head", "q4k_dense", "q5k_dense", "moe_t1", "moe_t4", "moe_t8"]
@@ -992,6 +1067,7 @@ def run_extras(args, rank, world, local_rank):
         gc.collect()
         torch.cuda.empty_cache()
     out["decode_1col"] = run_decode(args, rank, world, local_rank)
+    out["tensor_core"] = run_tensor_core(args, rank, world, local_rank)
     return out
 
 
