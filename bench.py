@@ -1073,10 +1073,13 @@ def run_extras(args, rank, world, local_rank):
 
 def run_case_for_profile(spec: str, launches: int):
     """One case, launched `launches` times eagerly (for ncu -k/-s/-c captures).
-    spec = fmt:ROWSxK:NCOLS, e.g. q6_k_planar:2560x10240:8."""
+    spec = fmt:ROWSxK:NCOLS[:tc], e.g. q6_k_planar:2560x10240:8 (":tc": with
+    MMVQ_FLAG_TENSOR_CORE)."""
     import torch
     from block_quantized_matvec_gb300 import mmvq, synth
-    fmt, shape, nc = spec.split(":")
+    parts = spec.split(":")
+    fmt, shape, nc = parts[:3]
+    flags = mmvq.FLAG_TENSOR_CORE if parts[3:] == ["tc"] else 0
     rows, K = (int(v) for v in shape.split("x"))
     nc = int(nc)
     t = {"q6_k_planar": mmvq.TYPE_Q6_K_PLANAR, "q6_k": mmvq.TYPE_Q6_K, "q4_k": mmvq.TYPE_Q4_K,
@@ -1087,7 +1090,7 @@ def run_case_for_profile(spec: str, launches: int):
     xq = mmvq.quantize_q8_1(torch.from_numpy(synth.activations(K, nc)).cuda())
     y = torch.empty((nc, rows), device="cuda")
     for _ in range(launches):
-        mmvq.gemv(t, W, rows, K, xq, nc, out=y)
+        mmvq.gemv(t, W, rows, K, xq, nc, out=y, flags=flags)
     torch.cuda.synchronize()
     print(json.dumps({"case": spec, "launches": launches, "y0": float(y[0, 0])}))
 
