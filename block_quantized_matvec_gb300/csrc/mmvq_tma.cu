@@ -15,7 +15,9 @@
 // the parity wait cannot alias an older phase.  A warp copies its tile's
 // lane bytes out of the ring with 16-byte shared loads (the tile order makes
 // them conflict-free), releases the stage, decodes and accumulates with
-// dp4a; the K-slices are summed in a fixed warp order.
+// dp4a; the K-slices are summed in a fixed warp order.  For 4-8 columns,
+// MMVQ_FLAG_TENSOR_CORE swaps in the tensor-core consumer of tma_mma.cuh
+// (same tiles, same staging, same launch shape, same bits).
 //
 // Weights are never written by a kernel of this library that lets its
 // successor launch early (repack and gather wait for completion), so the

@@ -1,8 +1,9 @@
 // The dense ring kernel over planar tiles (Q6_K, Q4_K, Q5_K), shared by the
 // translation units that instantiate it: mmvq_tma.cu (Q8_1 columns, with
-// and without a cluster K-split, and the parity-debug instance) and
-// mmvq_tma_f32.cu (fp32 columns quantised inside the kernel).  The design
-// notes are at the top of mmvq_tma.cu.
+// and without a cluster K-split, the parity-debug instance, and for 4-8
+// columns the tensor-core consumer's instances) and mmvq_tma_f32.cu (fp32
+// columns quantised inside the kernel).  The design notes are at the top of
+// mmvq_tma.cu.
 #pragma once
 #include "q8_1.cuh"
 #include "tma_mma.cuh"
