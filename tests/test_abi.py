@@ -156,6 +156,23 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert L.mmvq_selftest_grid_barrier_timeout(A, 0, None) == mmvq.ERR_SHAPE
 
 
+def test_flag_words_are_checked_on_host(lib):
+    L = lib
+    A = 0x10000
+    # mmvq_gemv_ex / mmvq_gemv_f32 / mmvq_debug_block_sums_ex: bits other than
+    # MMVQ_FLAG_XQ_STABLE (1) and MMVQ_FLAG_TENSOR_CORE (2) are rejected
+    assert mmvq.FLAG_XQ_STABLE == 1 and mmvq.FLAG_TENSOR_CORE == 2
+    for bad in (4, 8, 1 << 31, 3 | 4):
+        assert L.mmvq_gemv_ex(1014, A, 16, 256, A, 1, A, bad, None) == mmvq.ERR_SHAPE
+        assert L.mmvq_gemv_f32(1014, A, 16, 256, A, 256, 1, A, A, bad, None) == mmvq.ERR_SHAPE
+        assert L.mmvq_debug_block_sums_ex(1014, A, 16, 256, A, 1, A, A, bad, None) == mmvq.ERR_SHAPE
+    # the other rules come first, as for mmvq_debug_block_sums
+    assert L.mmvq_debug_block_sums_ex(1014, A, 16, 255, A, 1, A, A, 2, None) == mmvq.ERR_SHAPE
+    assert L.mmvq_debug_block_sums_ex(1014, A, 16, 256, A, 9, A, A, 2, None) == mmvq.ERR_NCOLS
+    assert L.mmvq_debug_block_sums_ex(1014, A, 16, 256, A, 1, A, None, 2, None) == mmvq.ERR_NULL
+    assert L.mmvq_debug_block_sums_ex(7, A, 16, 256, A, 1, A, A, 2, None) == mmvq.ERR_TYPE
+
+
 def test_product_package_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "block_quantized_matvec_gb300")
     for dirpath, _, files in os.walk(pkg):
