@@ -17,6 +17,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmmvq.so")
 BUILD_DIR = os.path.join(HERE, "_build")
+# The debug build: the same library with the ring kernels' device-side index
+# checks compiled in (MMVQ_CHECKED; a failed check sets bit 4 of the device
+# fault word and skips the access).  Built on request only.
+LIB_CHECKED = os.path.join(HERE, "libmmvq_checked.so")
+BUILD_DIR_CHECKED = os.path.join(HERE, "_build_checked")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-extended-lambda", "-Xcompiler", "-fPIC",
@@ -39,23 +44,28 @@ def _deps():
         [os.path.join(ROOT, "include", "mmvq.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Builds libmmvq.so (checked=True: the debug build, libmmvq_checked.so)
+    and returns its path."""
+    lib = LIB_CHECKED if checked else LIB
+    bdir = BUILD_DIR_CHECKED if checked else BUILD_DIR
+    flags = NVCC_FLAGS + (["-DMMVQ_CHECKED"] if checked else [])
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
+        cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -68,15 +78,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for _, err in results:
             print(err)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                checked="--checked" in sys.argv))

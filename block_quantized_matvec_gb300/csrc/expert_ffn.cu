@@ -137,6 +137,11 @@ __device__ __forceinline__ void ffn_stream(const GroupedRing& r, uint8_t* ring, 
     const int rg0 = rgb * G;
     const int nvalid = min(G, n_rg - rg0);
     const int pe = offs[grp + 1];
+    // debug build: the item's tiles lie inside its expert's weights
+    if (!MMVQ_INDEX_OK(grp >= 0 && rg0 >= 0 && rg0 + nvalid <= n_rg && spb * P <= nb)) {
+      *r.fail = 1;
+      break;
+    }
     for (int p0 = offs[grp]; p0 < pe && !*r.fail; p0 += CM) {
       for (int bb = 0; bb < spb; ++bb) {
         if (issued >= r.S && !mbar_wait(&r.empty[slot], par ^ 1u, 128)) {
@@ -269,6 +274,9 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
   uint8_t* xact = reinterpret_cast<uint8_t*>(red + C * kMaxCols * kTileRows);
   float* xda = reinterpret_cast<float*>(xact + (size_t)(CM <= 2 ? CM : 0) * act_row_bytes(H));
   float* xsa = xda + (CM <= 2 ? CM : 0) * nbq_h;
+  // debug build: the layout must fit the launch (the same outcome in every
+  // CTA, so none is left at a grid barrier)
+  if (!MMVQ_SMEM_OK(smem, xsa + (CM <= 2 ? CM : 0) * nbq_h)) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {

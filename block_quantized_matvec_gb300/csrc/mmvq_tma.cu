@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
   float* da = reinterpret_cast<float*>(act + (size_t)CM * rb);
   float* sa = da + CM * nbq;
   float* red = sa + CM * nbq;
+  // debug build: the layout must fit the launch
+  if (!MMVQ_SMEM_OK(smem, red + (size_t)C * kMaxCols * kTileRows)) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -147,6 +149,12 @@ __global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
         const int64_t rg0 = rgb * G;
         const int nvalid = (int)min((int64_t)G, n_rg - rg0);
         const int pe = offsets[grp + 1];
+        // debug build: the item's tiles lie inside its expert's weights
+        if (!MMVQ_INDEX_OK(expert_ids[grp] >= 0 && expert_ids[grp] < n_experts && rg0 >= 0 &&
+                           rg0 + nvalid <= n_rg && spb * P <= nb)) {
+          *r.fail = 1;
+          break;
+        }
         for (int p0 = offsets[grp]; p0 < pe && !*r.fail; p0 += CM) {
           for (int bb = 0; bb < spb; ++bb) {
             if (issued >= S && !mbar_wait(&r.empty[slot], par ^ 1u, 128)) {

@@ -19,6 +19,38 @@ static __device__ unsigned int g_fault_word = 0;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 constexpr int kFaultMbarTimeout = 1;
 
+// Debug build (compiled with MMVQ_CHECKED, libmmvq_checked.so): device-side
+// index checks in the ring kernels.  Each check tests an index or an extent
+// against the bounds of its buffer: the kernel's shared-memory layout
+// against the dynamic shared memory it was launched with, every bulk copy's
+// source range against the weights' extent, every tile a consumer reads
+// against the ring, every K-block it uses against the staged columns.  A
+// failed check sets bit 4 of this translation unit's fault word (read with
+// mmvq_read_device_fault), and the kernel skips the access and stops its
+// ring (whose bounded waits then end it): no trap, the context stays usable.
+// In the product build every check is the constant true and compiles away.
+constexpr int kFaultIndexCheck = 4;
+#ifdef MMVQ_CHECKED
+__device__ __forceinline__ bool index_ok(bool ok) {
+  if (!ok) atomicOr(&g_fault_word, kFaultIndexCheck);
+  return ok;
+}
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+// MMVQ_SMEM_OK(base, end): [base, end) lies inside the launch's dynamic
+// shared memory (base: its start).
+#define MMVQ_INDEX_OK(cond) ::mmvq::index_ok(cond)
+#define MMVQ_SMEM_OK(base, end) \
+  ::mmvq::index_ok((size_t)((const uint8_t*)(end) - (const uint8_t*)(base)) <= \
+                   (size_t)::mmvq::dynamic_smem_bytes())
+#else
+#define MMVQ_INDEX_OK(cond) true
+#define MMVQ_SMEM_OK(base, end) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -255,18 +287,20 @@ __device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot,
     }
     // a row group past the end reads a stale (in-bounds) tile and stores nothing
     const uint8_t* tile = r.ring + (size_t)s * r.stage_bytes + tile_off;
+    // debug build: the tile lies in the ring, its K-block in the staging
+    const bool in = MMVQ_INDEX_OK(s < r.S && tile_off + TB <= r.stage_bytes && bb * P + p < nbq / 8);
     if (LAYOUT == kQ4Planar) {
       Q4Half w;
-      load_q4_tile_smem(tile, lane, w);
+      if (in) load_q4_tile_smem(tile, lane, w);
       __syncwarp();
       if (lane == 0) mbar_arrive(&r.empty[s]);
-      if (valid) q4_dot<NC>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, nullptr, 0);
+      if (valid && in) q4_dot<NC>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, nullptr, 0);
     } else {
       Q6Half w;
-      load_q6_tile_smem(tile, lane, w);
+      if (in) load_q6_tile_smem(tile, lane, w);
       __syncwarp();
       if (lane == 0) mbar_arrive(&r.empty[s]);
-      if (valid) q6_dot<NC>(w, h, bb * P + p, act, rb, da, nbq, acc, nullptr, 0);
+      if (valid && in) q6_dot<NC>(w, h, bb * P + p, act, rb, da, nbq, acc, nullptr, 0);
     }
   }
 #pragma unroll

@@ -137,6 +137,11 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   float* xred = red + C * kMaxCols * kTileRows;
   uint64_t* xfull = reinterpret_cast<uint64_t*>(xred + (CS > 1 ? 2 * CS * G * NCOLS * kTileRows : 0));
   uint64_t* xempty = xfull + 2;
+  // debug build: the layout must fit the launch (the same outcome in every
+  // CTA of a cluster, so none is left at the cluster barrier)
+  if (!MMVQ_SMEM_OK(smem, CLUSTER ? reinterpret_cast<uint8_t*>(xempty + 2)
+                                  : reinterpret_cast<uint8_t*>(xred)))
+    return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -179,6 +184,12 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
         if (*fail) break;
         const int64_t left = my_rgs - j * G;
         const int valid = (int)(left < G ? left : G);
+        // debug build: the stage's tiles lie inside the weights
+        if (!MMVQ_INDEX_OK(cid + (j * G + valid - 1) * (int64_t)ncl < n_rg &&
+                           blk0 + (int64_t)(bb + 1) * P <= nb)) {
+          *fail = 1;
+          break;
+        }
         mbar_expect_tx(&full[slot], (uint32_t)(valid * P * TB));
         for (int g = 0; g < valid; ++g) {
           const int64_t rg = cid + (j * G + g) * (int64_t)ncl;
@@ -278,40 +289,42 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
       }
       const uint8_t* tile = ring + (size_t)s * stage_bytes + (size_t)warp * TB;
       const int64_t scs = rows * (K / kQK8);
+      // debug build: the tile lies in the ring, its K-block in the staging
+      const bool use = valid && MMVQ_INDEX_OK(s < S && warp < C && bb * P + p < nbc);
       if constexpr (MMA) {
         if (LAYOUT == kQ6Planar) {
           Q6Mma w;
-          if (valid) load_q6_mma(tile, mg, mt, w);
+          if (use) load_q6_mma(tile, mg, mt, w);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
-          if (valid) q6_mma<NCOLS, SUMI>(w, bb * P + p, lane, act, rb, tab, macc, msrow, scs);
+          if (use) q6_mma<NCOLS, SUMI>(w, bb * P + p, lane, act, rb, tab, macc, msrow, scs);
         } else {
           Q45Mma w;
-          if (valid) load_q45_mma<LAYOUT == kQ5Planar>(tile, mg, mt, w);
+          if (use) load_q45_mma<LAYOUT == kQ5Planar>(tile, mg, mt, w);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
-          if (valid)
+          if (use)
             q45_mma<NCOLS, LAYOUT == kQ5Planar, SUMI>(w, bb * P + p, lane, act, rb, tab, macc,
                                                       msrow, scs);
         }
       } else if (LAYOUT == kQ4Planar) {
         Q4Half w;
-        if (valid) load_q4_tile_smem(tile, lane, w);
+        if (use) load_q4_tile_smem(tile, lane, w);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q4_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
+        if (use) q4_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
       } else if (LAYOUT == kQ5Planar) {
         Q5Half w;
-        if (valid) load_q5_tile_smem(tile, lane, w);
+        if (use) load_q5_tile_smem(tile, lane, w);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q5_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
+        if (use) q5_dot<NCOLS>(w, h, bb * P + p, act, rb, da, sa, nbq, acc, srow, scs);
       } else {
         Q6Half w;
-        if (valid) load_q6_tile_smem(tile, lane, w);
+        if (use) load_q6_tile_smem(tile, lane, w);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (valid) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, scs);
+        if (use) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, scs);
       }
     }
     // halves of each row, then the group's K-slices in warp order

@@ -442,7 +442,9 @@ MMVQ_API int mmvq_launch_shape_ex(int type, int64_t rows, int K, int ncols, int3
  * on a shared-memory barrier, and of mmvq_expert_ffn on its grid barriers,
  * is bounded (about one second); a wait that runs out sets a bit here (1: a
  * shared-memory barrier wait timed out; 2: a grid barrier timed out) instead
- * of hanging, and the kernel returns with its outputs undefined.  Synchronises
+ * of hanging, and the kernel returns with its outputs undefined.  In the
+ * debug build (libmmvq_checked.so, compiled with MMVQ_CHECKED) bit 4 reports
+ * a failed device-side index check (the access was skipped).  Synchronises
  * `stream`, stores the word in *fault and clears it.  This HOST-pointer
  * call blocks; it is not part of the hot path.  No counterpart on the
  * pages (their kernels have no such waits).
