@@ -206,7 +206,8 @@ __host__ __device__ constexpr int tile_bytes(int layout) {
 // With a K-split over a cluster of CS CTAs each stages K/CS of the
 // activations and holds the exchange buffers [2][CS][G][ncols][16] floats
 // and two pairs of mbarriers.  mma: the tensor-core consumer's table of
-// 32 floats per 32-block (tma_mma.cuh).
+// 32 floats per 32-block (tma_mma.cuh).  The K-slice partials [C][8][16]
+// floats are double-buffered when P > 1.
 __host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int ncols, int G, int P,
                                                  int CS = 1, bool mma = false) {
   const int C = G * P;
@@ -215,7 +216,7 @@ __host__ __device__ inline size_t tma_smem_bytes(int layout, int S, int K, int n
                       (size_t)ncols * (Kc / kQK8) * 4 * (has_min(layout) ? 2 : 1) +
                       (mma ? (size_t)(Kc / kQK8) * 32 * 4 : 0);
   return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) + cols +
-         (size_t)C * kMaxCols * kTileRows * 4 +
+         (size_t)C * kMaxCols * kTileRows * 4 * (P > 1 ? 2 : 1) +
          (CS > 1 ? (size_t)2 * CS * G * ncols * kTileRows * 4 + 32 : 0);
 }
 
@@ -261,12 +262,17 @@ struct GroupedRing {
 };
 
 // One (item, chunk) for consumer warp (g, p): row group rg, K-slice p.
+// red: the K-slice partials, two buffers of [C][8][16] floats used in turn
+// (rpar, flipped by every call; all warps of a group make the same calls),
+// so one group barrier per call orders them: a warp writes a buffer again
+// only after the barrier of the next call, which the warp that read it
+// passes after reading.
 template <int LAYOUT, int NC>
 __device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot, uint32_t& par,
-                                                int g, int p, int P, int lane, int spb,
-                                                const uint8_t* act, int rb, const float* da,
-                                                const float* sa, int nbq, float* red,
-                                                float* ybase, int64_t rg, bool valid,
+                                                uint32_t& rpar, int g, int p, int P, int C,
+                                                int lane, int spb, const uint8_t* act, int rb,
+                                                const float* da, const float* sa, int nbq,
+                                                float* red, float* ybase, int64_t rg, bool valid,
                                                 int64_t rows) {
   constexpr int TB = tile_bytes(LAYOUT);
   const int i = lane & 15;
@@ -313,7 +319,8 @@ __device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot,
     }
     return;
   }
-  float* rg_red = red + (size_t)g * P * kMaxCols * kTileRows;
+  float* rg_red = red + ((size_t)(rpar & 1u) * C + (size_t)g * P) * kMaxCols * kTileRows;
+  rpar ^= 1u;
   if (h == 0) {
 #pragma unroll
     for (int c = 0; c < NC; ++c) rg_red[(p * kMaxCols + c) * kTileRows + i] = acc[c];
@@ -327,7 +334,6 @@ __device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot,
       ybase[c * rows + row] = sum;
     }
   }
-  group_sync(2 + g, 32 * P);
 }
 
 // Reads and clears this translation unit's fault word (the caller has

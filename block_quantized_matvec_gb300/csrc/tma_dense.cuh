@@ -131,10 +131,12 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
   float* da = reinterpret_cast<float*>(act + NCOLS * rb);
   float* sa = da + NCOLS * nbq;  // Q4_K only
   float* tab = sa + (has_min(LAYOUT) ? NCOLS * nbq : 0);  // MMA: [nbq][4][8]
+  // K-slice partials [C][8][16] floats, two buffers by batch parity when
+  // P > 1 (so one group barrier per batch orders them)
   float* red = tab + (MMA ? nbq * 32 : 0);
   // cluster exchange: xred [2][CS][G][NCOLS][16] floats (rank 0's is used),
   // then xfull[2], xempty[2]
-  float* xred = red + C * kMaxCols * kTileRows;
+  float* xred = red + C * kMaxCols * kTileRows * (P > 1 ? 2 : 1);
   uint64_t* xfull = reinterpret_cast<uint64_t*>(xred + (CS > 1 ? 2 * CS * G * NCOLS * kTileRows : 0));
   uint64_t* xempty = xfull + 2;
   // debug build: the layout must fit the launch (the same outcome in every
@@ -327,11 +329,15 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
         if (use) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, scs);
       }
     }
-    // halves of each row, then the group's K-slices in warp order
+    // halves of each row, then the group's K-slices in warp order.  The
+    // batch's partials buffer: a warp writes the buffer of batch j + 2 only
+    // after the group barrier of batch j + 1, which the warp that reads
+    // batch j's partials passes after reading them.
+    float* redj = red + (P > 1 ? (size_t)(j & 1) * C * kMaxCols * kTileRows : 0);
     if constexpr (MMA) {
       // the MMA lanes' row sums into the dp4a lanes' layout (row i, all
       // columns on lanes i and 16 + i), through this warp's partials
-      float* wred = red + (size_t)warp * kMaxCols * kTileRows;
+      float* wred = redj + (size_t)warp * kMaxCols * kTileRows;
       __syncwarp();
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
@@ -362,18 +368,17 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
       }
       if (h == 0) {
 #pragma unroll
-        for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
+        for (int c = 0; c < NCOLS; ++c) redj[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
       }
       group_sync(2 + g, 32 * P);
       if (p == 0 && valid && h == 0 && row < rows) {
 #pragma unroll
         for (int c = 0; c < NCOLS; ++c) {
           float sum = 0.0f;
-          for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
+          for (int q = 0; q < P; ++q) sum += redj[((g * P + q) * kMaxCols + c) * kTileRows + i];
           y[c * rows + row] = sum;
         }
       }
-      group_sync(2 + g, 32 * P);
     } else {
       // this CTA's sum over its P K-slices, then the cluster's K-slices:
       // ranks 1..CS-1 send, rank 0 adds in rank order
@@ -384,14 +389,14 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
       } else {
         if (h == 0) {
 #pragma unroll
-          for (int c = 0; c < NCOLS; ++c) red[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
+          for (int c = 0; c < NCOLS; ++c) redj[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
         }
         group_sync(2 + g, 32 * P);
 #pragma unroll
         for (int c = 0; c < NCOLS; ++c) {
           float sum = 0.0f;
           if (p == 0 && h == 0)
-            for (int q = 0; q < P; ++q) sum += red[((g * P + q) * kMaxCols + c) * kTileRows + i];
+            for (int q = 0; q < P; ++q) sum += redj[((g * P + q) * kMaxCols + c) * kTileRows + i];
           part[c] = sum;
         }
       }
@@ -432,7 +437,6 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
             mbar_arrive_cluster(cluster_map(&xempty[xb], lane));
         }
       }
-      if (P > 1) group_sync(2 + g, 32 * P);
     }
   }
 }
