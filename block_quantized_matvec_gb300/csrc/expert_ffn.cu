@@ -63,14 +63,14 @@ constexpr int kFfnMaxSlots = 256;
 
 // Shared memory of a CTA with C consumer warps: the ring (S stages of C
 // tiles), one group's staged columns (CM x max(H, F) quants, d and s), the
-// K-slice partials (two buffers, used in turn).
+// K-slice partials.
 // One or two tokens (CM <= 2) add the CTA's own Q8_1 of the hidden states
 // (CM x act_row_bytes(H) quants, d and s).
 __host__ __device__ inline size_t ffn_smem_bytes(int layout, int S, int H, int F, int CM, int C) {
   const int Km = H > F ? H : F;
   return tma_ring_offset(S) + (size_t)S * C * tile_bytes(layout) +
          (size_t)CM * act_row_bytes(Km) + (size_t)CM * (Km / kQK8) * 8 +
-         (size_t)2 * C * kMaxCols * kTileRows * 4 +
+         (size_t)C * kMaxCols * kTileRows * 4 +
          (CM <= 2 ? (size_t)CM * act_row_bytes(H) + (size_t)CM * (H / kQK8) * 8 : 0);
 }
 
@@ -188,7 +188,6 @@ __device__ __forceinline__ void ffn_consume(const GroupedRing& r, int& slot, uin
   int a = it0 / n_rgb;
   int rgb = it0 - a * n_rgb;
   int staged_grp = -1, staged_p0 = -1;
-  uint32_t rpar = 0;  // the partials buffer in turn (a grid barrier precedes each phase)
   for (int it = it0; it < it1; ++it) {
     const int grp = active[a];
     const int pe = offs[grp + 1];
@@ -205,8 +204,8 @@ __device__ __forceinline__ void ffn_consume(const GroupedRing& r, int& slot, uin
       }
       float* ybase = y + (size_t)p0 * rows;
 #define MMVQ_FC(NC)                                                                          \
-  grouped_consume<LAYOUT, NC>(r, slot, par, rpar, g, p, P, G * P, lane, spb, act, rb, da, sa, \
-                              nbq, red, ybase, rg, valid, rows)
+  grouped_consume<LAYOUT, NC>(r, slot, par, g, p, P, lane, spb, act, rb, da, sa, nbq, red, \
+                              ybase, rg, valid, rows)
       if constexpr (CM == 1) {
         MMVQ_FC(1);
       } else if constexpr (CM == 2) {
@@ -272,7 +271,7 @@ __global__ void __launch_bounds__(32 * (FC + 1), FC < 12 ? 3 : 1)
   float* red = sa + CM * (Km / kQK8);
   // T <= 2: the CTA's own Q8_1 of the hidden states, [T][act_row_bytes(H)]
   // quants, then d and s as floats [T][H/32] each
-  uint8_t* xact = reinterpret_cast<uint8_t*>(red + 2 * C * kMaxCols * kTileRows);
+  uint8_t* xact = reinterpret_cast<uint8_t*>(red + C * kMaxCols * kTileRows);
   float* xda = reinterpret_cast<float*>(xact + (size_t)(CM <= 2 ? CM : 0) * act_row_bytes(H));
   float* xsa = xda + (CM <= 2 ? CM : 0) * nbq_h;
   // debug build: the layout must fit the launch (the same outcome in every

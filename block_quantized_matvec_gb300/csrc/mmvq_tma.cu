@@ -55,7 +55,7 @@ __host__ __device__ inline size_t grouped_smem_bytes(int layout, int S, int K, i
                                                      int P) {
   return tma_ring_offset(S) + (size_t)S * G * P * tile_bytes(layout) +
          (size_t)CM * act_row_bytes(K) + (size_t)CM * (K / kQK8) * 8 +
-         (size_t)G * P * kMaxCols * kTileRows * 4 * 2;
+         (size_t)G * P * kMaxCols * kTileRows * 4;
 }
 
 template <int LAYOUT, int CM>
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
   float* sa = da + CM * nbq;
   float* red = sa + CM * nbq;
   // debug build: the layout must fit the launch
-  if (!MMVQ_SMEM_OK(smem, red + (size_t)2 * C * kMaxCols * kTileRows)) return;
+  if (!MMVQ_SMEM_OK(smem, red + (size_t)C * kMaxCols * kTileRows)) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -195,7 +195,6 @@ __global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
   const int p = warp - g * P;
   int slot = 0;
   uint32_t par = 0;
-  uint32_t rpar = 0;
   int staged_grp = -1, staged_p0 = -1;
   for (int64_t it = it0; it < it1; ++it) {
     const int grp = active[a];
@@ -222,8 +221,8 @@ __global__ void __launch_bounds__(13 * 32) mmvq_grouped_tma_kernel(
       }
       float* ybase = y + (size_t)p0 * rows;
 #define MMVQ_GC(NC)                                                                           \
-  grouped_consume<LAYOUT, NC>(r, slot, par, rpar, g, p, P, C, lane, spb, act, rb, da, sa, nbq, \
-                              red, ybase, rg, valid, rows)
+  grouped_consume<LAYOUT, NC>(r, slot, par, g, p, P, lane, spb, act, rb, da, sa, nbq, red, \
+                              ybase, rg, valid, rows)
       if constexpr (CM == 1) {
         MMVQ_GC(1);
       } else if constexpr (CM == 2) {

@@ -262,17 +262,12 @@ struct GroupedRing {
 };
 
 // One (item, chunk) for consumer warp (g, p): row group rg, K-slice p.
-// red: the K-slice partials, two buffers of [C][8][16] floats used in turn
-// (rpar, flipped by every call; all warps of a group make the same calls),
-// so one group barrier per call orders them: a warp writes a buffer again
-// only after the barrier of the next call, which the warp that read it
-// passes after reading.
 template <int LAYOUT, int NC>
 __device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot, uint32_t& par,
-                                                uint32_t& rpar, int g, int p, int P, int C,
-                                                int lane, int spb, const uint8_t* act, int rb,
-                                                const float* da, const float* sa, int nbq,
-                                                float* red, float* ybase, int64_t rg, bool valid,
+                                                int g, int p, int P, int lane, int spb,
+                                                const uint8_t* act, int rb, const float* da,
+                                                const float* sa, int nbq, float* red,
+                                                float* ybase, int64_t rg, bool valid,
                                                 int64_t rows) {
   constexpr int TB = tile_bytes(LAYOUT);
   const int i = lane & 15;
@@ -319,8 +314,7 @@ __device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot,
     }
     return;
   }
-  float* rg_red = red + ((size_t)(rpar & 1u) * C + (size_t)g * P) * kMaxCols * kTileRows;
-  rpar ^= 1u;
+  float* rg_red = red + (size_t)g * P * kMaxCols * kTileRows;
   if (h == 0) {
 #pragma unroll
     for (int c = 0; c < NC; ++c) rg_red[(p * kMaxCols + c) * kTileRows + i] = acc[c];
@@ -334,6 +328,7 @@ __device__ __forceinline__ void grouped_consume(const GroupedRing& r, int& slot,
       ybase[c * rows + row] = sum;
     }
   }
+  group_sync(2 + g, 32 * P);
 }
 
 // Reads and clears this translation unit's fault word (the caller has

@@ -329,15 +329,16 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
         if (use) q6_dot<NCOLS>(w, h, bb * P + p, act, rb, da, nbq, acc, srow, scs);
       }
     }
-    // halves of each row, then the group's K-slices in warp order.  The
-    // batch's partials buffer: a warp writes the buffer of batch j + 2 only
-    // after the group barrier of batch j + 1, which the warp that reads
-    // batch j's partials passes after reading them.
-    float* redj = red + (P > 1 ? (size_t)(j & 1) * C * kMaxCols * kTileRows : 0);
+    // halves of each row, then the group's K-slices in warp order.  With
+    // P > 1 the batch's partials go to buffer j % 2: a warp writes the
+    // buffer of batch j + 2 only after the group barrier of batch j + 1,
+    // which the warp that reads batch j's partials passes after reading
+    // them.
     if constexpr (MMA) {
       // the MMA lanes' row sums into the dp4a lanes' layout (row i, all
       // columns on lanes i and 16 + i), through this warp's partials
-      float* wred = redj + (size_t)warp * kMaxCols * kTileRows;
+      float* wred = red + (P > 1 ? (size_t)(j & 1) * C * kMaxCols * kTileRows : 0) +
+                    (size_t)warp * kMaxCols * kTileRows;
       __syncwarp();
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
@@ -366,6 +367,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
         }
         continue;
       }
+      float* redj = red + (size_t)(j & 1) * C * kMaxCols * kTileRows;
       if (h == 0) {
 #pragma unroll
         for (int c = 0; c < NCOLS; ++c) redj[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
@@ -387,6 +389,7 @@ __global__ void __launch_bounds__(13 * 32) mmvq_planar_tma_kernel(const uint8_t*
 #pragma unroll
         for (int c = 0; c < NCOLS; ++c) part[c] = acc[c];
       } else {
+        float* redj = red + (size_t)(j & 1) * C * kMaxCols * kTileRows;
         if (h == 0) {
 #pragma unroll
           for (int c = 0; c < NCOLS; ++c) redj[(warp * kMaxCols + c) * kTileRows + i] = acc[c];
