@@ -147,3 +147,17 @@ def test_flag_is_ignored_below_four_columns_and_by_gguf_types():
     Wg = dev(W)
     assert _same_bits(mmvq.gemv(mmvq.TYPE_Q6_K, Wg, rows, K, xqd, 6, flags=TC),
                       mmvq.gemv(mmvq.TYPE_Q6_K, Wg, rows, K, xqd, 6))
+
+
+def test_fp32_columns_with_the_flag():
+    # mmvq_gemv_f32 takes the quantiser and the product for the flag (its
+    # one-launch instance is a dp4a one): the same xq bytes and y bits
+    rows, K, ncols = 2560, 2560, 6
+    W = synth.q6_k_weights(rows, K, salt=12)
+    P = mmvq.repack_planar(dev(W), rows, K)
+    x = dev(synth.activations(K, ncols, salt=12))
+    y0, q0 = mmvq.gemv_f32(mmvq.TYPE_Q6_K_PLANAR, P, rows, K, x, ncols)
+    y1, q1 = mmvq.gemv_f32(mmvq.TYPE_Q6_K_PLANAR, P, rows, K, x, ncols, flags=TC)
+    assert np.array_equal(host(q0), host(q1))
+    assert _same_bits(y0, y1)
+    assert np.array_equal(host(q1), oracle.quantize_q8_1(host(x)))
